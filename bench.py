@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Attention-forward benchmark on GB300.
+
+One step = one fa_fwd call over the whole workload (every batch, head and
+query tile): O = softmax(scale QK^T [+mask]) V and LSE.  Default workload:
+B=8, H=16, Sq=Sk=2048, D=128, bf16, non-causal.  Metric: forward TFLOP/s
+(4*B*H*Sq*Sk*D, halved when causal) and its fraction of the measured dense
+bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 it runs under torch.distributed.run, one rank per GPU; every rank
+processes its own full workload (independent problems, no data-path
+collective: weak scaling) and value = all ranks' FLOPs / the slowest rank's
+time.  `--impl reference` times the fp64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd attention TFLOP/s & % of GB300 dense BF16 peak (causal FLOPs halved)"
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["exact_attention_82_gb300/csrc/fa_fwd_kernel.cu",
+                  "exact_attention_82_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_82_gb300/csrc/fa_internal.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, help="index into the workload table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target seconds of oracle work for the CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return None, "fallback"
+
+
+def traffic_per_launch(workload_name: str):
+    """DRAM bytes per launch from a committed ncu capture, if it still
+    describes the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload_name)
+    if not entry or entry.get("kernel_sha256") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [ln.strip().split(",") for ln in self.out.read().splitlines() if ln.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_82_gb300 as fa
+    from exact_attention_82_gb300.inputs import WORKLOADS, workload_qkv
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    q, k, v = workload_qkv(args.workload)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_fwd(dq, dk, dv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank).start()
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    st = fa.fa_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_strerror(st)}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))           # evict the previous step's data from L2
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    else:
+        ms = ms_local
+    st = fa.fa_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after timing: {fa.fa_strerror(st)}")
+
+    e2e = None if args.no_e2e else run_e2e(args, w, q, k, v, dev, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q, k, v, args.cpu_seconds)
+    if rank != 0:
+        return None
+    peaks, which = measured_peaks()
+    peak = float(peaks["bf16_tflops"]) if peaks else FALLBACK_PEAK_TFLOPS
+    tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
+    value = world * w.flops / (ms * 1e-3) / 1e12
+    traffic = traffic_per_launch(w.name)
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "desc": w.describe(), "B": w.B, "H": w.H, "Sq": w.Sq,
+                   "Sk": w.Sk, "D": w.D, "causal": w.causal,
+                   "parallelism": f"independent workload per GPU x{world}",
+                   "l2": "flushed before every step (256 MiB write outside the timed events)",
+                   "pct_of_bf16_peak": round(100.0 * tflops_launch / peak, 2),
+                   "wall_s_timed_region": round(t_wall, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(tflops_launch, 2),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops_launch / peak, 4),
+                     "peak_source": f"{which}: bf16_tflops (burst, cuBLAS bf16 GEMM)"
+                     if peaks else "fallback: 1.9 PFLOP/s bf16",
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "impl": "ours",
+    }
+
+
+def run_e2e(args, w, q, k, v, dev, world):
+    """Same metric through the public call with host buffers: every step copies
+    Q, K, V from pinned host memory, runs fa_fwd and reads O and LSE back."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_82_gb300 as fa
+
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
+    do = torch.empty_like(ho, device=dev)
+    dl = torch.empty_like(hl, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, o=do, lse=dl, scale=w.scale, causal=w.causal, stream=stream)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------- CPU (oracle) legs
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_sample(w, qb, kb, vb, heads):
+    """Oracle over the first `heads` (b,h) pairs, all rows; returns (seconds, flops)."""
+    import oracle
+
+    BH = w.B * w.H
+    qs = qb.reshape(BH, w.Sq, w.D)[:heads][None]
+    ks = kb.reshape(BH, w.Sk, w.D)[:heads][None]
+    vs = vb.reshape(BH, w.Sk, w.D)[:heads][None]
+    t0 = time.perf_counter()
+    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, nthreads=_host_cores())
+    dt = time.perf_counter() - t0
+    return dt, w.flops / BH * heads
+
+
+def cpu_baseline(w, q, k, v, target_s):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    same workload: whole heads, grown until about `target_s` seconds."""
+    from exact_attention_82_gb300.inputs import bf16_bits
+
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    cores = _host_cores()
+    BH = w.B * w.H
+    heads = min(BH, cores)
+    dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+    if dt < target_s / 4 and heads < BH:
+        heads = min(BH, max(heads + 1, int(heads * target_s / max(dt, 1e-3) * 0.8)))
+        dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{heads} of {BH} (batch,head) pairs of {w.name}, every query row; "
+                      f"fp64 C oracle with S and P materialised"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    sample (whole heads) of the same workload."""
+    from exact_attention_82_gb300.inputs import WORKLOADS, bf16_bits, workload_qkv
+
+    w = WORKLOADS[args.workload]
+    q, k, v = workload_qkv(args.workload)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    cores = _host_cores()
+    heads = min(w.B * w.H, cores)
+    # size a step to about 3 s of host work, from the first warm-up step
+    dt, _ = _oracle_sample(w, qb, kb, vb, heads)
+    heads = max(1, min(w.B * w.H, int(heads * 3.0 / max(dt, 1e-3))))
+    for _ in range(args.warmup - 1):
+        _oracle_sample(w, qb, kb, vb, heads)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"{heads} of {w.B * w.H} (batch,head) pairs of {w.name} per step, every query "
+              f"row; fp64 C oracle, S and P materialised")
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "desc": w.describe()},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
+              file=sys.stderr)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        res = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

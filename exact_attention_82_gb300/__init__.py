@@ -1,1 +1,143 @@
-"""GB300-native FlashAttention-2-style attention forward (placeholder; the binding follows)."""
+"""GB300-native (sm_103a) FlashAttention-2-style attention forward.
+
+The compute lives in ``_build/libfa_gb300.so`` (hand-written CUDA: TMA,
+tcgen05 MMAs into tensor memory, online softmax).  This module is a thin
+ctypes binding with the C ABI's names (``include/fa.h``): it only marshals
+arguments.  torch is used for device memory and streams.  There is no CPU
+or library fallback: if the shared library cannot be built or loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_strerror", "fa_device_status",
+           "fa_selftest_bounded_wait", "fa_version", "FAError", "lib", "library_path",
+           "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
+           "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
+           "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW"]
+
+FA_OK = 0
+FA_ERR_NULLPTR = -1
+FA_ERR_BAD_SHAPE = -2
+FA_ERR_UNSUPPORTED_D = -3
+FA_ERR_UNSUPPORTED_CAUSAL = -4
+FA_ERR_MISALIGNED = -5
+FA_ERR_BAD_SCALE = -6
+FA_ERR_CUDA = -7
+FA_ERR_TIMEOUT = -8
+FA_ERR_ALIAS = -9
+FA_ERR_BAD_WINDOW = -10
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+# name -> (restype, argtypes), mirroring include/fa.h
+_SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
+    "fa_strerror": (ctypes.c_char_p, [_i]),
+    "fa_device_status": (_i, [_vp]),
+    "fa_selftest_bounded_wait": (_i, [_i, _vp]),
+    "fa_version": (_i, []),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = fa_strerror(status)
+        super().__init__(f"{where}: {msg} (status {status})" if where else msg)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded shared library (built in-tree with nvcc on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            handle = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def fa_strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def fa_version() -> int:
+    return lib().fa_version()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+               Sq: int, Sk: int, D: int, scale: float, causal: int, stream_ptr: int) -> int:
+    """The C call with raw device pointers; returns the status code."""
+    return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
+                        int(causal), stream_ptr)
+
+
+def fa_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
+           stream=None):
+    """Attention forward on torch CUDA tensors.
+
+    q: bf16 [B,H,Sq,D]; k, v: bf16 [B,H,Sk,D] (contiguous, same device).
+    o (bf16 [B,H,Sq,D]) and lse (fp32 [B,H,Sq]) are allocated if not given.
+    scale defaults to 1/sqrt(D).  Launches on ``stream`` (default: torch's
+    current stream) and returns (o, lse) without synchronising.
+    """
+    import torch
+
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if o is None:
+        o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    if tuple(o.shape) != (B, H, Sq, D) or tuple(lse.shape) != (B, H, Sq):
+        raise ValueError("o must be [B, H, Sq, D] and lse [B, H, Sq]")
+    if scale is None:
+        scale = D ** -0.5
+    st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, H, Sq, Sk, D, scale, int(bool(causal)), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_device_status(stream=None) -> int:
+    """Synchronise the stream, return and clear the kernels' status word."""
+    return lib().fa_device_status(_stream_ptr(stream))
+
+
+def fa_selftest_bounded_wait(timeout_us: int, stream=None) -> int:
+    return lib().fa_selftest_bounded_wait(int(timeout_us), _stream_ptr(stream))

@@ -1,0 +1,38 @@
+// fa_internal.h -- declarations shared by the C-ABI layer and the kernels'
+// translation unit.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kBlockM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBlockN = 128;  // keys per K/V tile
+
+// Runtime parameters of one forward launch.
+struct FwdParams {
+    float *lse;        // [B*H, Sq] fp32
+    int Sq, Sk;
+    int n_mblk;        // ceil(Sq / kBlockM)
+    int n_kv;          // ceil(Sk / kBlockN)
+    int causal;
+    float scale_log2;  // scale * log2(e)
+    unsigned long long timeout_ns;  // bound of every on-chip wait
+};
+
+// Dynamic shared memory the forward kernel for head dim D asks for.
+int fwd_smem_bytes(int D);
+
+// Launch the forward kernel for head dim D (64 or 128) over n_ctas tiles.
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                       const CUtensorMap &tm_v, const CUtensorMap &tm_o, const FwdParams &p,
+                       long long n_ctas, cudaStream_t stream);
+
+// Device status word: read it (after synchronising `stream`) and reset it.
+cudaError_t status_read_and_clear(int *out, cudaStream_t stream);
+
+// One CTA waiting on a barrier nothing arrives on, bounded by limit_ns.
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,112 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host before touching the GPU.  No GPU needed."""
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import exact_attention_82_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# harmless fake device addresses: the calls below fail validation first
+A = 1 << 20
+A2 = 1 << 30
+A3 = 1 << 34
+A4 = 1 << 38
+A5 = 1 << 40
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_strerror", "fa_device_status", "fa_selftest_bounded_wait",
+              "fa_version"):
+        assert n in names
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_library_exports_declared_symbol(name):
+    lib = fa.lib()
+    assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_library_is_in_tree():
+    assert os.path.commonpath([fa.library_path(), ROOT]) == ROOT
+    assert os.path.exists(fa.library_path())
+
+
+def test_version_and_strerror():
+    assert fa.fa_version() >= 100
+    for code in range(0, -11, -1):
+        s = fa.fa_strerror(code)
+        assert s and s != "unknown status", code
+    assert fa.fa_strerror(12345) == "unknown status"
+
+
+def call(q=A, k=A2, v=A3, o=A4, lse=A5, B=1, H=1, Sq=128, Sk=128, D=64, scale=0.125, causal=0):
+    return fa.fa_fwd_raw(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, 0)
+
+
+def test_null_pointers():
+    assert call(q=0) == fa.FA_ERR_NULLPTR
+    assert call(lse=0) == fa.FA_ERR_NULLPTR
+
+
+def test_misaligned():
+    assert call(k=A2 + 8) == fa.FA_ERR_MISALIGNED
+    assert call(lse=A5 + 4) == fa.FA_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(Sq=0), dict(Sk=-1)])
+def test_bad_shape(kw):
+    assert call(**kw) == fa.FA_ERR_BAD_SHAPE
+
+
+@pytest.mark.parametrize("D", [0, 32, 96, 256])
+def test_unsupported_d(D):
+    assert call(D=D) == fa.FA_ERR_UNSUPPORTED_D
+
+
+def test_causal_rules():
+    assert call(causal=1, Sq=128, Sk=256) == fa.FA_ERR_UNSUPPORTED_CAUSAL
+    assert call(causal=2) == fa.FA_ERR_UNSUPPORTED_CAUSAL
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), 0.0, -0.5])
+def test_bad_scale(scale):
+    assert call(scale=scale) == fa.FA_ERR_BAD_SCALE
+
+
+def test_alias():
+    # o overlapping q (both 1*1*128*64*2 bytes = 16 KiB)
+    assert call(o=A + 4096) == fa.FA_ERR_ALIAS
+    assert call(lse=A4 + 16) == fa.FA_ERR_ALIAS
+
+
+def test_selftest_argument_check():
+    assert fa.fa_selftest_bounded_wait(0, stream=0) == fa.FA_ERR_BAD_SHAPE
+    assert fa.fa_selftest_bounded_wait(2_000_000, stream=0) == fa.FA_ERR_BAD_SHAPE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path only")
+def test_valid_call_without_gpu_reports_cuda_error():
+    assert call() == fa.FA_ERR_CUDA
+    assert "CUDA error" in fa.fa_strerror(fa.FA_ERR_CUDA)
+
+
+def test_torch_wrapper_rejects_cpu_tensors():
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, o=q.clone(), lse=torch.zeros(1, 1, 128), stream=0)

@@ -1,0 +1,140 @@
+"""GPU parity: the sm_103a kernel, called through the C ABI, against the fp64
+oracle on the same seeded bf16 inputs, element by element (small and
+mid-size shapes spanning several tiles and a ragged tail) and on sampled rows
+at the five full workload sizes, in the launch configuration the benchmark
+times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_82_gb300 as fa
+from exact_attention_82_gb300.inputs import SEED_BASE, WORKLOADS, bf16_bits, make_qkv, workload_qkv
+from parity_util import compare, full_parity, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    """Every test must leave the on-device status word at FA_OK."""
+    yield
+    assert fa.fa_device_status() == fa.FA_OK
+
+
+# ------------------------------------------------------------ small / ragged
+SMALL = [
+    # B, H, Sq, Sk, D
+    (1, 1, 128, 128, 64),
+    (1, 1, 128, 128, 128),
+    (1, 1, 1, 1, 64),
+    (1, 1, 1, 1, 128),
+    (1, 1, 2, 2, 64),
+    (3, 1, 63, 63, 128),
+    (1, 3, 64, 64, 64),
+    (1, 1, 65, 65, 128),
+    (3, 3, 127, 127, 64),
+    (1, 3, 129, 129, 128),
+    (2, 3, 389, 389, 128),
+    (1, 2, 1000, 1000, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_parity_small(shape, causal):
+    B, H, Sq, Sk, D = shape
+    full_parity(B, H, Sq, Sk, D, causal, seed=1000 + sum(shape))
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 300), (200, 70), (128, 1), (300, 511), (77, 1024)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_parity_rectangular_noncausal(Sq, Sk, D):
+    full_parity(2, 2, Sq, Sk, D, False, seed=Sq * 7 + Sk)
+
+
+def test_parity_peaky_softmax():
+    """Q x4 (the peaky workload's recipe) at a small size, both head dims."""
+    for D in (64, 128):
+        full_parity(2, 2, 300, 300, D, True, seed=77, q_mult=4.0)
+
+
+def test_parity_other_scale():
+    full_parity(1, 2, 257, 257, 128, False, seed=5, scale=0.3)
+
+
+# --------------------------------------------------- the five workloads
+@pytest.mark.parametrize("index", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
+def test_parity_workload(index):
+    w = WORKLOADS[index]
+    q, k, v = workload_qkv(index)
+    og, lg = run_gpu(q, k, v, w.scale, w.causal)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    if w.B * w.H * w.Sq <= 4096:
+        orf, lrf = oracle.attn_fwd(qb, kb, vb, w.scale, w.causal)
+        compare(og, lg, orf, lrf, w.name)
+        return
+    bh, rows = sample_rows(w.B, w.H, w.Sq, n_random=160, seed=index)
+    orf, lrf = oracle.attn_fwd_rows(qb, kb, vb, bh, rows, w.scale, w.causal)
+    og2 = og.reshape(w.B * w.H, w.Sq, w.D)[bh, rows]
+    lg2 = lg.reshape(w.B * w.H, w.Sq)[bh, rows]
+    compare(og2, lg2, orf, lrf, w.name + " (sampled rows)")
+    # properties that hold at any size: O is a convex combination of V rows
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
+    vmax = v.float().amax(dim=2, keepdim=True).double().numpy()
+    vmin = v.float().amin(dim=2, keepdim=True).double().numpy()
+    assert np.all(og <= vmax + 2e-2) and np.all(og >= vmin - 2e-2)
+
+
+# ------------------------------------------------------------- properties
+def test_deterministic_bitwise():
+    q, k, v = (t.cuda() for t in make_qkv(2, 4, 777, 777, 128, seed=3))
+    o1, l1 = fa.fa_fwd(q, k, v, causal=True)
+    o2, l2 = fa.fa_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_guard_bands_untouched():
+    """Outputs carved out of larger buffers: bytes around O and LSE keep their canary."""
+    B, H, S, D = 2, 3, 300, 64
+    q, k, v = (t.cuda() for t in make_qkv(B, H, S, S, D, seed=4))
+    pad = 4096
+    n_o = B * H * S * D
+    obuf = torch.full((n_o + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((B * H * S + 2 * pad,), -3.0, dtype=torch.float32, device="cuda")
+    o = obuf[pad:pad + n_o].view(B, H, S, D)
+    lse = lbuf[pad:pad + B * H * S].view(B, H, S)
+    fa.fa_fwd(q, k, v, o=o, lse=lse, causal=True)
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:pad] == 7.0) and torch.all(obuf[pad + n_o:] == 7.0)
+    assert torch.all(lbuf[:pad] == -3.0) and torch.all(lbuf[pad + B * H * S:] == -3.0)
+    ref_o, ref_l = oracle.attn_fwd(*(bf16_bits(t.cpu()) for t in (q, k, v)), D ** -0.5, True)
+    compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), ref_o, ref_l, "guard")
+
+
+def test_side_stream():
+    s = torch.cuda.Stream()
+    q, k, v = make_qkv(1, 2, 200, 200, 128, seed=8)
+    with torch.cuda.stream(s):
+        og, lg = run_gpu(q, k, v, 128 ** -0.5, False, stream=s)
+    ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), 128 ** -0.5, False)
+    compare(og, lg, *ref, "side stream")
+
+
+def test_identical_v_rows_on_gpu():
+    q, k, v = make_qkv(1, 2, 256, 256, 128, seed=9)
+    v = v[:, :, :1].expand_as(v).contiguous()
+    og, _ = run_gpu(q, k, v, 128 ** -0.5, False)
+    want = v[:, :, :1].float().double().numpy()
+    assert np.max(np.abs(og - want)) <= 2e-2
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A wait nothing satisfies ends after its limit with FA_ERR_TIMEOUT in the
+    status word; the context stays usable."""
+    assert fa.fa_device_status() == fa.FA_OK
+    assert fa.fa_selftest_bounded_wait(20_000) == fa.FA_OK  # 20 ms limit
+    assert fa.fa_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_device_status() == fa.FA_OK  # cleared by the read
+    full_parity(1, 1, 128, 128, 64, False, seed=1)  # context still works
