@@ -102,7 +102,7 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
     if (!isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
     const long long BH = (long long)B * H;
-    const long long n_mblk = (Sq + fa::kBlockM - 1) / fa::kBlockM;
+    const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
     const long long n_ctas = n_mblk * BH;
     if (BH > (1ll << 31) || n_ctas > 0x7fffffffll) return FA_ERR_BAD_SHAPE;
     const size_t q_bytes = (size_t)BH * Sq * D * 2, kv_bytes = (size_t)BH * Sk * D * 2;

@@ -4,26 +4,43 @@
 // log-sum-exp, with the online softmax of the source walk-through
 // "FlashAttention-2 相比 FlashAttention-1，到底改了什么", section
 // "第二处源码差异：kernel 主循环怎么组织" (running row max m, running sum l,
-// acc rescaled by exp(m - m_new), one division by l at the end).
+// acc rescaled by exp(m - m_new), a single division by l at the end).
 //
-// How it maps onto the chip (one CTA per 128-row query tile, the grid of the
-// same page's section "第一处源码差异：launch grid 怎么铺": query blocks x
-// batch x heads):
-//   warp 4     TMA producer: the Q tile once, then K_j and V_j tiles into a
-//              two-stage shared-memory ring (128-byte swizzle);
-//   warp 5     allocates tensor memory and issues the tcgen05 MMAs from one
-//              thread: S_j = Q K_j^T into one of two TMEM S buffers, and
-//              O += P_j V_j into the TMEM O accumulator;
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t), reads its S
-//              row from TMEM, masks (first tile only), updates m and l,
-//              writes P_j (bf16) to shared memory, rescales its O row in
-//              TMEM when m grew, and in the epilogue multiplies O by 1/l,
+// Mapping onto the chip.  The grid is (query blocks x batch x heads), the
+// launch shape of the same page's section "第一处源码差异：launch grid 怎么铺";
+// each CTA owns 256 query rows as two 128-row sub-tiles t = 0, 1, which share
+// every K/V tile:
+//   warps 10-11 idle (they complete the third warpgroup, whose registers go
+//              to the softmax warpgroups);
+//   warp 9     TMA producer: Q0 and Q1 once, then K_j and V_j into two
+//              shared-memory rings (128-byte swizzle), K kept one tile ahead;
+//   warp 8     allocates all 512 tensor-memory (TMEM) columns and issues the
+//              tcgen05 MMAs from one thread, in the order
+//                S0_j = Q0 K_j^T,  O1 += P1_{j+1} V_{j+1},  S1_j = Q1 K_j^T,
+//                O0 += P0_j V_j
+//              so that while the tensor core works on one sub-tile the other
+//              sub-tile's softmax runs (each softmax has two MMAs of slack);
+//   warps 0-3  softmax of sub-tile 0, warps 4-7 of sub-tile 1: thread r owns
+//              query row r (TMEM lane r): it reads its S row from TMEM, masks
+//              (only on its first key tile), updates the running max and sum,
+//              writes P (bf16) back over its S row in TMEM, where the P V MMA
+//              reads it as its A operand, and at the end scales O by 1/l,
 //              stages it in shared memory for a TMA store and writes LSE.
-// Key/value tiles run from the last one to the first, so the only tile that
-// needs masking (the causal diagonal or the ragged last tile) comes first,
-// as in the page's split into masking steps then unmasked steps; tiles
-// wholly above the causal diagonal are never visited ("FlashAttention-2 —
-// L3 Cross-Paper Synthesis", §3 item 4).
+// TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
+// the first 64 columns of S_t (128 bf16 packed in pairs).
+//
+// The running max is only moved when a row's max grows by more than 2^8 (in
+// exp2 units): P and l keep using the stale max, which is exact because O and
+// l are divided by the same factor at the end, and it takes the O rescale off
+// almost every iteration ("reduce non-matmul work", same page, section
+// "第四处差异：v2 减少非 matmul 开销").  O_t is stable while sub-tile t is
+// between "S_t full" and "P_t full" (S_t is issued after the previous P_t V),
+// so the softmax thread rescales its own O row there when needed.
+//
+// Key tiles run from the last one to the first, so the only tile of a
+// sub-tile that needs masking (causal diagonal or ragged last tile) is its
+// first, and tiles wholly above the causal diagonal are never visited
+// ("FlashAttention-2 — L3 Cross-Paper Synthesis", §3 item 4).
 //
 // Every barrier wait is bounded in time; a wait that gives up records a
 // status code and the CTA winds down without trapping.
@@ -40,52 +57,55 @@ __device__ int g_status_word = 0;
 
 template <int D>
 struct FwdCfg {
-    static constexpr int BM = kBlockM, BN = kBlockN, STAGES = 2;
-    static constexpr int NCH = D / 64;                       // 64-column (128-byte) chunks
-    static constexpr uint32_t Q_BYTES = BM * D * 2;
-    static constexpr uint32_t KV_BYTES = BN * D * 2;         // one K or one V tile
-    static constexpr uint32_t P_BYTES = BM * BN * 2;
-    static constexpr uint32_t Q_CHUNK = BM * 128;            // bytes per 64-col chunk
-    static constexpr uint32_t KV_CHUNK = BN * 128;
+    static constexpr int BM = kBlockM;  // rows per sub-tile (TMEM lanes)
+    static constexpr int BN = kBlockN;  // keys per K/V tile
+    static constexpr int KST = (D == 128) ? 3 : 4;
+    static constexpr int VST = (D == 128) ? 2 : 4;
+    static constexpr int NCH = D / 64;                    // 128-byte column chunks per row
+    static constexpr uint32_t QT_BYTES = BM * D * 2;      // one query sub-tile
+    static constexpr uint32_t KV_BYTES = BN * D * 2;      // one K or V tile
+    static constexpr uint32_t CHUNK = 128 * 128;          // 128 rows x 128 bytes
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr uint32_t USED = OFF_BAR + BAR_BYTES;
-    // + alignment slack; at least 120 KB so that one CTA occupies an SM
-    // (each CTA takes all 512 TMEM columns)
-    static constexpr uint32_t SMEM = (USED + 1024 > 120 * 1024) ? USED + 1024 : 120 * 1024;
+    static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+    static constexpr uint32_t TM_O = 256;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "atoms");
+    static_assert(BM == 128 && BN == 128, "tile");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(SMEM > 114 * 1024, "one CTA per SM (it takes all TMEM columns)");
 };
 
 // barrier slots (8 bytes each) inside the OFF_BAR block
 enum : uint32_t {
     B_Q_FULL = 0,
-    B_K_FULL = 1,   // + stage (2)
-    B_K_EMPTY = 3,  // + stage
-    B_V_FULL = 5,   // + stage
-    B_V_EMPTY = 7,  // + stage
-    B_S_FULL = 9,   // + buffer (2)
-    B_S_FREE = 11,  // + buffer
-    B_P_FULL = 13,
-    B_O_DONE = 14,
-    B_DRAIN = 15,
-    N_BARS = 16
+    B_K_FULL = 1,    // + stage (up to 4)
+    B_K_EMPTY = 5,   // + stage
+    B_V_FULL = 9,    // + stage
+    B_V_EMPTY = 13,  // + stage
+    B_S_FULL = 17,   // + sub-tile
+    B_P_FULL = 19,   // + sub-tile
+    B_O_DONE = 21,   // + sub-tile
+    B_DRAIN = 23,
 };
-constexpr uint32_t SLOT_TMEM = 160;   // byte offset of the TMEM base address
-constexpr uint32_t SLOT_ABORT = 164;  // byte offset of the abort flag
+constexpr uint32_t SLOT_TMEM = 200;   // byte offset of the TMEM base address
+constexpr uint32_t SLOT_ABORT = 204;  // byte offset of the abort flag
 constexpr unsigned long long kDrainNs = 20ull * 1000 * 1000;  // 20 ms
+constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+2 idle)
+// Register split.  At launch every thread has 168 (3 warps per SM sub-partition);
+// the MMA/TMA warpgroup drops to 56 and the softmax warpgroups rise to 224:
+// 256 x 224 + 128 x 56 = 64512 = 384 x 168, the block's launch total.
+constexpr uint32_t kRegsSoftmax = 224, kRegsOther = 56;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
@@ -102,15 +122,22 @@ __global__ void __launch_bounds__(192, 1)
     const int mi = (int)(blockIdx.x % (unsigned)p.n_mblk);
     const int bh = (int)(blockIdx.x / (unsigned)p.n_mblk);
     const int mblk = p.causal ? (p.n_mblk - 1 - mi) : mi;  // causal: longest first
-    int j_hi = p.n_kv - 1;
-    if (p.causal) j_hi = min(j_hi, (mblk * C::BM + C::BM - 1) / C::BN);
-    const int n_iter = j_hi + 1;
+    const int row0 = mblk * 2 * C::BM;
+    bool act[2];
+    int jhi[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        act[t] = row0 + t * C::BM < p.Sq;
+        jhi[t] = p.n_kv - 1;
+        if (p.causal) jhi[t] = min(jhi[t], (row0 + t * C::BM + C::BM - 1) / C::BN);
+    }
+    const int J = act[1] ? max(jhi[0], jhi[1]) : jhi[0];  // first key tile of the CTA
+    const int N = J + 1;                                  // key tiles the CTA loads
     const bool mask_first = p.causal || (p.Sk % C::BN) != 0;
 
     const uint32_t sQ = sbase + C::OFF_Q;
     const uint32_t sK = sbase + C::OFF_K;
     const uint32_t sV = sbase + C::OFF_V;
-    const uint32_t sP = sbase + C::OFF_P;
     const uint32_t bars = sbase + C::OFF_BAR;
     auto bar = [&](uint32_t i) { return bars + 8u * i; };
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + SLOT_ABORT);
@@ -118,23 +145,24 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q_FULL), 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::KST; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_S_FREE + s), 128);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_S_FULL + t), 1);
+            mbar_init(bar(B_P_FULL + t), 128);
+            mbar_init(bar(B_O_DONE + t), 1);
         }
-        mbar_init(bar(B_P_FULL), 128);
-        mbar_init(bar(B_O_DONE), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 8) {
         tmem_alloc(sbase + C::OFF_BAR + SLOT_TMEM, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -144,237 +172,256 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
     const unsigned long long tlim = p.timeout_ns;
 
-    if (warp == 4) {
+    auto wait = [&](uint32_t b, uint32_t parity) {
+        return mbar_wait(bar(b), parity, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT);
+    };
+
+    if (warp >= 10) {
+        regs_decrease<kRegsOther>();  // idle warps: give their registers away
+    } else if (warp == 9) {
         // ===================================================== TMA producer
+        regs_decrease<kRegsOther>();
         if (lane == 0) {
             tma_prefetch_map(&tm_q);
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(B_Q_FULL), C::Q_BYTES);
-            for (int c = 0; c < C::NCH; ++c)
-                tma_load_3d(sQ + c * C::Q_CHUNK, &tm_q, c * 64, mblk * C::BM, bh, bar(B_Q_FULL), pol_q);
-            int issued = 0;
-            for (int it = 0; it < n_iter; ++it) {
-                const int j = j_hi - it;
-                const int st = it % C::STAGES;
-                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-                if (!mbar_wait(bar(B_K_EMPTY + st), ph ^ 1u, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT))
-                    break;
+            mbar_arrive_expect_tx(bar(B_Q_FULL), (act[1] ? 2u : 1u) * C::QT_BYTES);
+            for (int t = 0; t < 2; ++t)
+                if (act[t])
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * 64, row0 + t * C::BM, bh,
+                                    bar(B_Q_FULL), pol_q);
+            int nk = 0, nv = 0;  // loads issued
+            auto load_k = [&](int it) -> bool {
+                const int st = it % C::KST;
+                if (!wait(B_K_EMPTY + st, ((uint32_t)(it / C::KST) & 1u) ^ 1u)) return false;
                 mbar_arrive_expect_tx(bar(B_K_FULL + st), C::KV_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sK + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_k, c * 64, j * C::BN, bh,
+                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tm_k, c * 64, (J - it) * C::BN, bh,
                                 bar(B_K_FULL + st), pol_kv);
-                if (!mbar_wait(bar(B_V_EMPTY + st), ph ^ 1u, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT)) {
-                    issued = it * 2 + 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar(B_V_FULL + st), C::KV_BYTES);
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sV + st * C::KV_BYTES + c * C::KV_CHUNK, &tm_v, c * 64, j * C::BN, bh,
-                                bar(B_V_FULL + st), pol_kv);
-                issued = it * 2 + 2;
-            }
-            // wind down: every copy this thread issued has landed before the
-            // CTA may exit (already true on the normal path)
-            mbar_wait_drain(bar(B_Q_FULL), 0, kDrainNs);
-            for (int t = (issued > 4 ? issued - 4 : 0); t < issued; ++t) {
-                const int it = t >> 1;
-                const int st = it % C::STAGES;
-                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-                mbar_wait_drain(bar(((t & 1) ? B_V_FULL : B_K_FULL) + st), ph, kDrainNs);
-            }
-        }
-    } else if (warp == 5) {
-        // ======================================================= MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT);
-            auto issue_pv = [&](int t) -> bool {
-                const int st = t % C::STAGES;
-                const uint32_t ph = (uint32_t)(t / C::STAGES) & 1u;
-                if (!mbar_wait(bar(B_P_FULL), (uint32_t)t & 1u, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT))
-                    return false;
-                if (!mbar_wait(bar(B_V_FULL + st), ph, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT))
-                    return false;
-                tc_fence_after();
-                const uint32_t vbase = sV + st * C::KV_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    // A = P (K-major, 64-column chunks of 128 rows)
-                    const uint64_t ad = sw128_desc(sP + (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32, 16, 1024);
-                    // B = V (MN-major: D contiguous; 16 key rows per step)
-                    const uint64_t bd = sw128_desc(vbase + kk * 2048, C::KV_CHUNK, 1024);
-                    tc_mma_ss(tmem + C::TM_O, ad, bd, C::IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(bar(B_O_DONE));
-                tc_commit(bar(B_V_EMPTY + st));
+                nk = it + 1;
                 return true;
             };
-            for (int it = 0; ok && it < n_iter; ++it) {
-                const int st = it % C::STAGES;
-                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-                const int sb = it & 1;
-                const uint32_t sph = (uint32_t)(it >> 1) & 1u;
-                ok = mbar_wait(bar(B_K_FULL + st), ph, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT) &&
-                     mbar_wait(bar(B_S_FREE + sb), sph ^ 1u, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kbase = sK + st * C::KV_BYTES;
-                const uint32_t s_tmem = tmem + (sb ? C::TM_S1 : C::TM_S0);
+            auto load_v = [&](int it) -> bool {
+                const int st = it % C::VST;
+                if (!wait(B_V_EMPTY + st, ((uint32_t)(it / C::VST) & 1u) ^ 1u)) return false;
+                mbar_arrive_expect_tx(bar(B_V_FULL + st), C::KV_BYTES);
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tm_v, c * 64, (J - it) * C::BN, bh,
+                                bar(B_V_FULL + st), pol_kv);
+                nv = it + 1;
+                return true;
+            };
+            bool ok = load_k(0);
+            for (int it = 0; ok && it < N; ++it) {
+                if (it + 1 < N) ok = load_k(it + 1);
+                if (ok) ok = load_v(it);
+            }
+            // wind down: every copy issued here has landed before the CTA may exit
+            mbar_wait_drain(bar(B_Q_FULL), 0, kDrainNs);
+            for (int it = (nk > C::KST ? nk - C::KST : 0); it < nk; ++it)
+                mbar_wait_drain(bar(B_K_FULL + it % C::KST), (uint32_t)(it / C::KST) & 1u, kDrainNs);
+            for (int it = (nv > C::VST ? nv - C::VST : 0); it < nv; ++it)
+                mbar_wait_drain(bar(B_V_FULL + it % C::VST), (uint32_t)(it / C::VST) & 1u, kDrainNs);
+        }
+    } else if (warp == 8) {
+        // ======================================================= MMA issuer
+        regs_decrease<kRegsOther>();
+        if (lane == 0) {
+            bool ok = wait(B_Q_FULL, 0);
+            int npv[2] = {0, 0};  // P V products issued per sub-tile
+            auto part = [&](int t, int it) { return act[t] && (J - it) <= jhi[t]; };
+            auto issue_s = [&](int t, int sk) {
+                const uint32_t qb = sQ + t * C::QT_BYTES;
+                const uint32_t kb = sK + sk * C::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = sw128_desc(sQ + (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sw128_desc(kbase + (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32, 16, 1024);
-                    tc_mma_ss(s_tmem, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+                    tc_mma_ss(tmem + t * 128, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                              C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(B_S_FULL + sb));
-                tc_commit(bar(B_K_EMPTY + st));
-                if (it > 0) ok = issue_pv(it - 1);
+                tc_commit(bar(B_S_FULL + t));
+            };
+            auto issue_pv = [&](int t, int it) -> bool {
+                const int sv = it % C::VST;
+                if (!wait(B_P_FULL + t, (uint32_t)npv[t] & 1u)) return false;
+                if (!wait(B_V_FULL + sv, (uint32_t)(it / C::VST) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t vb = sV + sv * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    // A = P_t in TMEM (8 columns = 16 keys per step); B = V, MN-major
+                    tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8,
+                              sw128_desc(vb + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
+                              (npv[t] > 0 || kk > 0) ? 1u : 0u);
+                ++npv[t];
+                return true;
+            };
+            for (int it = 0; ok && it < N; ++it) {
+                const int sk = it % C::KST;
+                ok = wait(B_K_FULL + sk, (uint32_t)(it / C::KST) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const bool p0 = part(0, it), p1 = part(1, it);
+                if (p0) issue_s(0, sk);
+                if (it > 0 && part(1, it - 1)) {
+                    ok = issue_pv(1, it - 1);
+                    if (!ok) break;
+                    tc_commit(bar(B_V_EMPTY + (it - 1) % C::VST));
+                }
+                if (p1) issue_s(1, sk);
+                tc_commit(bar(B_K_EMPTY + sk));
+                if (p0) {
+                    ok = issue_pv(0, it);
+                    if (!ok) break;
+                    if (it == N - 1) tc_commit(bar(B_O_DONE + 0));
+                    if (!p1) tc_commit(bar(B_V_EMPTY + it % C::VST));
+                }
             }
-            if (ok) issue_pv(n_iter - 1);
-            // wind down: all MMAs issued here are complete before TMEM is freed
+            if (ok && part(1, N - 1)) {
+                ok = issue_pv(1, N - 1);
+                if (ok) {
+                    tc_commit(bar(B_O_DONE + 1));
+                    tc_commit(bar(B_V_EMPTY + (N - 1) % C::VST));
+                }
+            }
+            // wind down: every MMA issued here is complete before TMEM is freed
             tc_commit(bar(B_DRAIN));
             mbar_wait_drain(bar(B_DRAIN), 0, kDrainNs);
         }
     } else {
-        // ============================================ softmax warpgroup
-        const int row = threadIdx.x;  // 0..127 == TMEM lane
-        const int row_g = mblk * C::BM + row;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // ============================================ softmax warpgroups
+        regs_increase<kRegsSoftmax>();
+        const int t = warp >> 2;          // sub-tile
+        const bool my_act = t ? act[1] : act[0];
+        const int my_jhi = t ? jhi[1] : jhi[0];
+        const int row = threadIdx.x & 127;  // row in the sub-tile == TMEM lane
+        const int row_g = row0 + t * C::BM + row;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_off + t * 128;
+        const uint32_t o_tm = tmem + lane_off + C::TM_O + t * D;
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY;  // running max of the raw scores q.k
-        float l_run = 0.f;        // running sum of exp2((s - m) * scale*log2e)
+        float m_used = -INFINITY;  // max in exp2 units (raw score * scale*log2e) used for P
+        float l_run = 0.f;         // sum of P over the keys seen, relative to m_used
         bool ok = true;
-        for (int it = 0; it < n_iter; ++it) {
-            const int sb = it & 1;
-            const uint32_t sph = (uint32_t)(it >> 1) & 1u;
-            ok = mbar_wait(bar(B_S_FULL + sb), sph, abort_flag, tlim, &g_status_word, FA_ERR_TIMEOUT);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t s[4][32];
-            const uint32_t s_tmem = tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, s[c]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-            tc_fence_before();
-            mbar_arrive(bar(B_S_FREE + sb));
-
-            if (it == 0 && mask_first) {
-                const int col0 = j_hi * C::BN;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int col = col0 + c * 32 + e;
-                        if (col >= p.Sk || (p.causal && col > row_g)) s[c][e] = __float_as_uint(-INFINITY);
-                    }
-            }
-            float mx = m_run;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
-            const float neg_m = -mx * sl2;
-            float sum = 0.f;
-            uint32_t pk[4][16];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, neg_m));
-                    sum += p0 + p1;
-                    pk[c][e] = pack_bf16x2(p0, p1);
-                }
-            const float alpha = ex2_approx((m_run - mx) * sl2);  // 0 on the first tile
-            l_run = l_run * alpha + sum;
-            m_run = mx;
-
-            if (it > 0) {
-                // O holds P_{it-1} V_{it-1}; it must be complete before O is
-                // rescaled and before the P buffer is overwritten
-                ok = mbar_wait(bar(B_O_DONE), (uint32_t)(it - 1) & 1u, abort_flag, tlim, &g_status_word,
-                               FA_ERR_TIMEOUT);
+        if (my_act) {
+            const int n_t = my_jhi + 1;
+            for (int i = 0; i < n_t; ++i) {
+                ok = wait(B_S_FULL + t, (uint32_t)i & 1u);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    const uint32_t o_tmem = tmem + lane_off + C::TM_O;
+                uint32_t s[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                if (i == 0 && mask_first) {
+                    // keys allowed for this row in this tile: columns [0, lim)
+                    const int end = p.causal ? min(p.Sk, row_g + 1) : p.Sk;
+                    const int lim = end - my_jhi * C::BN;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+                const float mxs = mx * sl2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
+                    const float m_new = fmaxf(m_used, mxs);
+                    alpha = ex2_approx(m_used - m_new);  // 0 on the first tile
+                    m_used = m_new;
+                    rescale = i > 0;
+                }
+                const float neg_m = -m_used;
+                float sum = 0.f;
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e]), sl2, neg_m));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, neg_m));
+                        sum += p0 + p1;
+                        pk[c * 16 + e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_tm + c * 16, &pk[c * 16]);
+                }
+                tmem_st_wait64(pk);
+                l_run = l_run * alpha + sum;
+                if (rescale) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(o_tmem + c * 32, o);
+                        tmem_ld32(o_tm + c * 32, o);
                         tmem_ld_wait(o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(o_tmem + c * 32, o);
+                        tmem_st32(o_tm + c * 32, o);
                         tmem_st_wait(o);
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(bar(B_P_FULL + t));
             }
-            // P row -> shared memory, K-major with the 128-byte swizzle:
-            // 16-byte unit U of the row goes to chunk U/8, unit (U%8)^(row%8)
-#pragma unroll
-            for (int U = 0; U < 16; ++U) {
-                const uint32_t addr = sP + (U >> 3) * C::Q_CHUNK + row * 128 + ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
-                st_shared_v4(addr, pk[U >> 2][(U & 3) * 4 + 0], pk[U >> 2][(U & 3) * 4 + 1],
-                             pk[U >> 2][(U & 3) * 4 + 2], pk[U >> 2][(U & 3) * 4 + 3]);
+            if (ok) {
+                ok = wait(B_O_DONE + t, 0);
+                ok = __all_sync(0xffffffffu, ok);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_P_FULL));
         }
-        if (ok) {
-            ok = mbar_wait(bar(B_O_DONE), (uint32_t)(n_iter - 1) & 1u, abort_flag, tlim, &g_status_word,
-                           FA_ERR_TIMEOUT);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        // all four warps agree before the shared epilogue barrier
-        named_bar_sync(1, 128);
+        named_bar_sync(1 + t, 128);
         const bool all_ok = (*abort_flag == 0u);
-        if (ok && all_ok) {
+        if (my_act && ok && all_ok) {
+            // ---- epilogue: O / l -> bf16 -> shared (this sub-tile's Q buffer,
+            // free once its last MMA is done) -> TMA store; LSE
             tc_fence_after();
             const float inv_l = 1.f / l_run;
-            const uint32_t o_tmem = tmem + lane_off + C::TM_O;
-            const uint32_t sO = sP;  // the P buffer is free once the last P V is done
+            const uint32_t sO = sQ + t * C::QT_BYTES;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(o_tmem + c * 32, o);
+                tmem_ld32(o_tm + c * 32, o);
                 tmem_ld_wait(o);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int U = c * 4 + u;  // 16-byte unit (8 columns) of the output row
+                    const int U = c * 4 + u;  // 16-byte unit (8 columns) of the row
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         w[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv_l,
                                            __uint_as_float(o[u * 8 + 2 * e + 1]) * inv_l);
-                    const uint32_t addr = sO + (U >> 3) * C::Q_CHUNK + row * 128 + ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
+                    const uint32_t addr = sO + (U >> 3) * C::CHUNK + row * 128 +
+                                          ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
                     st_shared_v4(addr, w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1 + t, 128);
             if (row == 0) {
 #pragma unroll
-                for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, sO + c * C::Q_CHUNK, c * 64, mblk * C::BM, bh);
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, row0 + t * C::BM, bh);
                 bulk_commit_group();
                 bulk_wait_group_read0();
             }
-            if (row_g < p.Sq) {
-                const float lse2 = m_run * sl2 + lg2_approx(l_run);  // log2 of sum exp
-                p.lse[(size_t)bh * p.Sq + row_g] = lse2 * 0.69314718055994531f;
-            }
+            if (row_g < p.Sq)
+                p.lse[(size_t)bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 8) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
@@ -405,11 +452,11 @@ template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas,
                                 cudaStream_t stream) {
-    static_assert(FwdCfg<D>::SMEM > 0, "");
     cudaError_t e = cudaFuncSetAttribute(fa_fwd_sm103a<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FwdCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    fa_fwd_sm103a<D><<<dim3((unsigned)n_ctas), dim3(192), FwdCfg<D>::SMEM, stream>>>(tm_q, tm_k, tm_v, tm_o, p);
+    fa_fwd_sm103a<D><<<dim3((unsigned)n_ctas), dim3(kThreads), FwdCfg<D>::SMEM, stream>>>(tm_q, tm_k, tm_v,
+                                                                                        tm_o, p);
     return cudaGetLastError();
 }
 

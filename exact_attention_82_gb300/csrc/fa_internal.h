@@ -7,14 +7,15 @@
 
 namespace fa {
 
-constexpr int kBlockM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBlockM = 128;  // query rows per sub-tile (TMEM lanes)
+constexpr int kCtaRows = 2 * kBlockM;  // query rows per CTA (two sub-tiles)
 constexpr int kBlockN = 128;  // keys per K/V tile
 
 // Runtime parameters of one forward launch.
 struct FwdParams {
     float *lse;        // [B*H, Sq] fp32
     int Sq, Sk;
-    int n_mblk;        // ceil(Sq / kBlockM)
+    int n_mblk;        // ceil(Sq / kCtaRows)
     int n_kv;          // ceil(Sk / kBlockN)
     int causal;
     float scale_log2;  // scale * log2(e)
