@@ -328,11 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
                 }
-                float mx = -INFINITY;
+                // row max: four independent chains of three-input max
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+                    for (int e = 0; e < 32; e += 8)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]), __uint_as_float(s[c][e + 2 * q + 1]));
+                const float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3]));
                 const float mxs = mx * sl2;
                 float alpha = 1.f;
                 bool rescale = false;
@@ -342,20 +347,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used = m_new;
                     rescale = i > 0;
                 }
-                const float neg_m = -m_used;
-                float sum = 0.f;
+                // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
+                // row sum in four packed partial sums
+                const uint64_t c2 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(-m_used, -m_used);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pk[64];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e]), sl2, neg_m));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, neg_m));
-                        sum += p0 + p1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])), c2, nm2),
+                                  x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
                         pk[c * 16 + e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(s_tm + c * 16, &pk[c * 16]);
                 }
+                float a0, a1, b0, b1;
+                f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+                f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+                const float sum = (a0 + a1) + (b0 + b1);
                 tmem_st_wait64(pk);
                 l_run = l_run * alpha + sum;
                 if (rescale) {
