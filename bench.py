@@ -87,6 +87,24 @@ def traffic_per_launch(workload_name: str):
     return entry.get("dram_bytes_per_launch")
 
 
+# ----------------------------------------------------- rank aggregation
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the slowest rank's step time); x itself at N=1."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Every rank processes its own full workload: all ranks' FLOPs / the slowest time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -188,12 +206,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    else:
-        ms = ms_local
+    ms = max_over_ranks(ms_local, world, dev)
     st = fa.fa_device_status(stream)
     if st != fa.FA_OK:
         raise RuntimeError(f"device status after timing: {fa.fa_strerror(st)}")
@@ -207,7 +220,7 @@ def run_ours(args, rank, world, local_rank):
     peaks, which = measured_peaks()
     peak = float(peaks["bf16_tflops"]) if peaks else FALLBACK_PEAK_TFLOPS
     tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(w.flops, world, ms)
     traffic = traffic_per_launch(w.name)
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -271,14 +284,10 @@ def run_e2e(args, w, q, k, v, dev, world):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-    return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(whole_job_tflops(w.flops, world, ms), 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
