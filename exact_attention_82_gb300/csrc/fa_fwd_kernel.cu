@@ -328,52 +328,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
                 }
-                // row max: four independent chains of three-input max
-                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // P is computed against the max already in use.  The row max is
+                // only taken on the first tile, or again for a tile whose sum shows
+                // a score more than 2^64 above that max (the sum also catches inf
+                // and NaN): then the tile is redone against its true max.  S is
+                // still intact in TMEM then, because P is stored after the check.
+                const uint64_t c2 = f2_pack(sl2, sl2);
+                float alpha = 1.f, sum = 0.f;
+                uint32_t pk[64];
+                auto take_max = [&]() {
+                    // row max: four independent chains of three-input max
+                    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8)
+                        for (int e = 0; e < 32; e += 8)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]), __uint_as_float(s[c][e + 2 * q + 1]));
-                const float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-                const float mxs = mx * sl2;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
-                    const float m_new = fmaxf(m_used, mxs);
+                            for (int q = 0; q < 4; ++q)
+                                mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
+                                              __uint_as_float(s[c][e + 2 * q + 1]));
+                    const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
                     alpha = ex2_approx(m_used - m_new);  // 0 on the first tile
                     m_used = m_new;
-                    rescale = i > 0;
-                }
-                // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
-                // row sum in four packed partial sums
-                const uint64_t c2 = f2_pack(sl2, sl2);
-                const uint64_t nm2 = f2_pack(-m_used, -m_used);
-                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-                uint32_t pk[64];
+                };
+                auto exp_pass = [&]() {
+                    // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
+                    // row sum in four packed partial sums
+                    const uint64_t nm2 = f2_pack(-m_used, -m_used);
+                    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])), c2, nm2),
-                                  x0, x1);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
-                        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-                        pk[c * 16 + e] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st16(s_tm + c * 16, &pk[c * 16]);
+                        for (int e = 0; e < 16; ++e) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
+                                             c2, nm2),
+                                      x0, x1);
+                            const float p0 = ex2_approx(x0);
+                            const float p1 = ex2_approx(x1);
+                            acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+                            pk[c * 16 + e] = pack_bf16x2(p0, p1);
+                        }
+                    float a0, a1, b0, b1;
+                    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+                    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+                    sum = (a0 + a1) + (b0 + b1);
+                };
+                if (i == 0) take_max();
+                exp_pass();
+                const bool redo = i > 0 && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
+                if (redo) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                    take_max();
+                    exp_pass();
                 }
-                float a0, a1, b0, b1;
-                f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
-                f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-                const float sum = (a0 + a1) + (b0 + b1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
                 tmem_st_wait64(pk);
                 l_run = l_run * alpha + sum;
-                if (rescale) {
+                if (redo) {
+                    // O holds the earlier tiles relative to the old max: rescale it
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -393,14 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);
             }
         }
+        // ---- epilogue: O / l -> bf16 -> shared memory (this sub-tile's Q
+        // buffer, free once its last MMA is done) -> TMA store; LSE.  Both
+        // named barriers run whatever `ok` says, so no warp can be left waiting.
         named_bar_sync(1 + t, 128);
-        const bool all_ok = (*abort_flag == 0u);
-        if (my_act && ok && all_ok) {
-            // ---- epilogue: O / l -> bf16 -> shared (this sub-tile's Q buffer,
-            // free once its last MMA is done) -> TMA store; LSE
+        const uint32_t sO = sQ + t * C::QT_BYTES;
+        if (my_act && ok) {
             tc_fence_after();
             const float inv_l = 1.f / l_run;
-            const uint32_t sO = sQ + t * C::QT_BYTES;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -420,17 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1 + t, 128);
-            if (row == 0) {
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, row0 + t * C::BM, bh);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-            }
-            if (row_g < p.Sq)
-                p.lse[(size_t)bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
         }
+        named_bar_sync(1 + t, 128);
+        if (my_act && ok && row == 0 && *abort_flag == 0u) {
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+                tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, row0 + t * C::BM, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+        }
+        if (my_act && ok && row_g < p.Sq)
+            p.lse[(size_t)bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
     }
 
     tc_fence_before();

@@ -138,3 +138,28 @@ def test_bounded_wait_gives_up_and_reports():
     assert fa.fa_device_status() == fa.FA_ERR_TIMEOUT
     assert fa.fa_device_status() == fa.FA_OK  # cleared by the read
     full_parity(1, 1, 128, 128, 64, False, seed=1)  # context still works
+
+
+def _growing_scores(D, lift, causal):
+    """Keys of the first key tile (index 0, processed last) score `lift` (in
+    exp2 units) above every other key, so later tiles outgrow the max taken
+    from the first tile processed."""
+    B, H, S = 1, 2, 384
+    q, k, v = make_qkv(B, H, S, S, D, seed=21)
+    q = torch.ones_like(q)  # every score is (scale) * sum(k_j)
+    target = lift * (D ** 0.5) / 1.4426950408889634 / D  # per-element key value
+    k = k * 0.05
+    k[:, :, :128] = (k[:, :, :128].float() + target).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lift", [40.0, 70.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scores_growing_past_first_tile_max(D, lift, causal):
+    """Large late scores: P grows to ~2^40 against the first tile's max (kept),
+    or past 2^64 (the tile is redone against its true max, O rescaled)."""
+    q, k, v = _growing_scores(D, lift, causal)
+    og, lg = run_gpu(q, k, v, D ** -0.5, causal)
+    ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), D ** -0.5, causal)
+    compare(og, lg, *ref, f"lift {lift} D{D}")
