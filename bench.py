@@ -178,7 +178,11 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        fa.fa_fwd(dq, dk, dv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+        if w.window_left >= 0:
+            fa.fa_fwd_window(dq, dk, dv, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
+                             stream=stream)
+        else:
+            fa.fa_fwd(dq, dk, dv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
 
     def barrier():
         if world > 1:
@@ -228,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "desc": w.describe(), "B": w.B, "H": w.H, "Sq": w.Sq,
-                   "Sk": w.Sk, "D": w.D, "causal": w.causal,
+                   "Sk": w.Sk, "D": w.D, "causal": w.causal, "window": list(w.window),
                    "parallelism": f"independent workload per GPU x{world}",
                    "l2": "flushed before every step (256 MiB write outside the timed events)",
                    "pct_of_bf16_peak": round(100.0 * tflops_launch / peak, 2),
@@ -268,7 +272,11 @@ def run_e2e(args, w, q, k, v, dev, world):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq, dk, dv, o=do, lse=dl, scale=w.scale, causal=w.causal, stream=stream)
+        if w.window_left >= 0:
+            fa.fa_fwd_window(dq, dk, dv, w.window[0], w.window[1], o=do, lse=dl, scale=w.scale,
+                             stream=stream)
+        else:
+            fa.fa_fwd(dq, dk, dv, o=do, lse=dl, scale=w.scale, causal=w.causal, stream=stream)
         ho.copy_(do, non_blocking=True)
         hl.copy_(dl, non_blocking=True)
 
@@ -309,7 +317,7 @@ def _oracle_sample(w, qb, kb, vb, heads):
     ks = kb.reshape(BH, w.Sk, w.D)[:heads][None]
     vs = vb.reshape(BH, w.Sk, w.D)[:heads][None]
     t0 = time.perf_counter()
-    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, nthreads=_host_cores())
+    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, w.window, nthreads=_host_cores())
     dt = time.perf_counter() - t0
     return dt, w.flops / BH * heads
 

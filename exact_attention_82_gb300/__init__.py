@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["fa_fwd", "fa_fwd_raw", "fa_strerror", "fa_device_status",
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_strerror", "fa_device_status",
            "fa_selftest_bounded_wait", "fa_version", "FAError", "lib", "library_path",
            "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
@@ -41,6 +41,8 @@ _i = ctypes.c_int
 # name -> (restype, argtypes), mirroring include/fa.h
 _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
+    "fa_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
+                           _vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
@@ -99,15 +101,15 @@ def fa_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: 
                         int(causal), stream_ptr)
 
 
-def fa_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
-           stream=None):
-    """Attention forward on torch CUDA tensors.
+def fa_fwd_window_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                      H: int, Sq: int, Sk: int, D: int, scale: float, window_left: int,
+                      window_right: int, stream_ptr: int) -> int:
+    """The windowed C call with raw device pointers; returns the status code."""
+    return lib().fa_fwd_window(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
+                               int(window_left), int(window_right), stream_ptr)
 
-    q: bf16 [B,H,Sq,D]; k, v: bf16 [B,H,Sk,D] (contiguous, same device).
-    o (bf16 [B,H,Sq,D]) and lse (fp32 [B,H,Sq]) are allocated if not given.
-    scale defaults to 1/sqrt(D).  Launches on ``stream`` (default: torch's
-    current stream) and returns (o, lse) without synchronising.
-    """
+
+def _prepare(q, k, v, o, lse):
     import torch
 
     B, H, Sq, D = q.shape
@@ -125,12 +127,40 @@ def fa_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool =
         raise ValueError("k and v must be [B, H, Sk, D] matching q")
     if tuple(o.shape) != (B, H, Sq, D) or tuple(lse.shape) != (B, H, Sq):
         raise ValueError("o must be [B, H, Sq, D] and lse [B, H, Sq]")
+    return o, lse, B, H, Sq, Sk, D
+
+
+def fa_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
+           stream=None):
+    """Attention forward on torch CUDA tensors.
+
+    q: bf16 [B,H,Sq,D]; k, v: bf16 [B,H,Sk,D] (contiguous, same device).
+    o (bf16 [B,H,Sq,D]) and lse (fp32 [B,H,Sq]) are allocated if not given.
+    scale defaults to 1/sqrt(D).  Launches on ``stream`` (default: torch's
+    current stream) and returns (o, lse) without synchronising.
+    """
+    o, lse, B, H, Sq, Sk, D = _prepare(q, k, v, o, lse)
     if scale is None:
         scale = D ** -0.5
     st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                     B, H, Sq, Sk, D, scale, int(bool(causal)), _stream_ptr(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_window(q, k, v, window_left: int, window_right: int, o=None, lse=None,
+                  scale: float | None = None, stream=None):
+    """Banded attention: key j allowed for query i iff i-window_left <= j <= i+window_right
+    (-1 = unbounded on that side).  Same tensors and return value as fa_fwd."""
+    o, lse, B, H, Sq, Sk, D = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = D ** -0.5
+    st = fa_fwd_window_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, H, Sq, Sk, D, scale, window_left, window_right,
+                           _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_window")
     return o, lse
 
 

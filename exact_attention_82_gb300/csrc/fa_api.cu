@@ -81,7 +81,7 @@ extern "C" const char *fa_strerror(int status) {
         case FA_ERR_CUDA: s = "CUDA error"; break;
         case FA_ERR_TIMEOUT: s = "an on-chip wait gave up (bounded-wait timeout)"; break;
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
-        case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1"; break;
+        case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1, and a bounded window needs Sq == Sk"; break;
         default: s = "unknown status"; break;
     }
     if (status == FA_ERR_CUDA && t_last_cuda != cudaSuccess)
@@ -91,19 +91,17 @@ extern "C" const char *fa_strerror(int status) {
     return t_errbuf;
 }
 
-extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
-                      int Sk, int D, float scale, int causal, void *stream) {
+// Checks shared by the forward entry points; FA_OK when the call may launch.
+static int check_fwd(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
+                     int Sq, int Sk, int D, float scale) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULLPTR;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_MISALIGNED;
     if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FA_ERR_BAD_SHAPE;
     if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
-    if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED_CAUSAL;
-    if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
     if (!isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
     const long long BH = (long long)B * H;
-    const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
-    const long long n_ctas = n_mblk * BH;
+    const long long n_ctas = ((Sq + fa::kCtaRows - 1) / fa::kCtaRows) * BH;
     if (BH > (1ll << 31) || n_ctas > 0x7fffffffll) return FA_ERR_BAD_SHAPE;
     const size_t q_bytes = (size_t)BH * Sq * D * 2, kv_bytes = (size_t)BH * Sk * D * 2;
     const size_t lse_bytes = (size_t)BH * Sq * 4;
@@ -112,25 +110,53 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
         overlaps(lse, lse_bytes, k, kv_bytes) || overlaps(lse, lse_bytes, v, kv_bytes) ||
         overlaps(lse, lse_bytes, o, q_bytes))
         return FA_ERR_ALIAS;
-    if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
+    return FA_OK;
+}
 
+// Encode the maps and launch; arguments already checked.  Key j is allowed
+// for query i iff i - wl <= j <= i + wr (a negative bound: unbounded).
+static int launch_checked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
+                          int Sk, int D, float scale, int wl, int wr, void *stream) {
+    if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
+    const long long BH = (long long)B * H;
+    const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
     if (!encode_bhsd(&tm_q, q, D, Sq, BH, fa::kBlockM) || !encode_bhsd(&tm_k, k, D, Sk, BH, fa::kBlockN) ||
         !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
         return fail_cuda(cudaErrorInvalidValue);
-
     fa::FwdParams p;
     p.lse = lse;
     p.Sq = Sq;
     p.Sk = Sk;
     p.n_mblk = (int)n_mblk;
     p.n_kv = (Sk + fa::kBlockN - 1) / fa::kBlockN;
-    p.causal = causal;
+    p.causal = (wr >= 0 && wl < 0) ? 1 : 0;  // triangular work: longest blocks first
+    p.wl = wl < 0 ? -1 : wl;
+    p.wr = wr < 0 ? -1 : wr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kWaitLimitNs;
-    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, n_ctas, (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, n_mblk * BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
+}
+
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
+                      int Sk, int D, float scale, int causal, void *stream) {
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
+    return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, -1, causal ? 0 : -1, stream);
+}
+
+extern "C" int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                             int Sq, int Sk, int D, float scale, int window_left, int window_right,
+                             void *stream) {
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (window_left < -1 || window_right < -1) return FA_ERR_BAD_WINDOW;
+    if ((window_left >= 0 || window_right >= 0) && Sq != Sk) return FA_ERR_BAD_WINDOW;
+    return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream);
 }
 
 extern "C" int fa_device_status(void *stream) {

@@ -123,17 +123,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = (int)(blockIdx.x / (unsigned)p.n_mblk);
     const int mblk = p.causal ? (p.n_mblk - 1 - mi) : mi;  // causal: longest first
     const int row0 = mblk * 2 * C::BM;
+    // key tiles [jlo, jhi] a sub-tile needs: those meeting some row's window
     bool act[2];
-    int jhi[2];
+    int jhi[2], jlo[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        act[t] = row0 + t * C::BM < p.Sq;
+        const int r_first = row0 + t * C::BM, r_last = r_first + C::BM - 1;
+        act[t] = r_first < p.Sq;
         jhi[t] = p.n_kv - 1;
-        if (p.causal) jhi[t] = min(jhi[t], (row0 + t * C::BM + C::BM - 1) / C::BN);
+        if (p.wr >= 0) jhi[t] = min(jhi[t], (r_last + p.wr) / C::BN);
+        jlo[t] = (p.wl >= 0) ? max(0, (r_first - p.wl) / C::BN) : 0;
     }
     const int J = act[1] ? max(jhi[0], jhi[1]) : jhi[0];  // first key tile of the CTA
-    const int N = J + 1;                                  // key tiles the CTA loads
-    const bool mask_first = p.causal || (p.Sk % C::BN) != 0;
+    const int J_lo = jlo[0];                              // sub-tile 0 reaches lowest
+    const int N = J - J_lo + 1;                           // key tiles the CTA loads
 
     const uint32_t sQ = sbase + C::OFF_Q;
     const uint32_t sK = sbase + C::OFF_K;
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             bool ok = wait(B_Q_FULL, 0);
             int npv[2] = {0, 0};  // P V products issued per sub-tile
-            auto part = [&](int t, int it) { return act[t] && (J - it) <= jhi[t]; };
+            auto part = [&](int t, int it) { return act[t] && (J - it) <= jhi[t] && (J - it) >= jlo[t]; };
             auto issue_s = [&](int t, int sk) {
                 const uint32_t qb = sQ + t * C::QT_BYTES;
                 const uint32_t kb = sK + sk * C::KV_BYTES;
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it > 0 && part(1, it - 1)) {
                     ok = issue_pv(1, it - 1);
                     if (!ok) break;
+                    if (J - (it - 1) == jlo[1]) tc_commit(bar(B_O_DONE + 1));  // its last tile
                     tc_commit(bar(B_V_EMPTY + (it - 1) % C::VST));
                 }
                 if (p1) issue_s(1, sk);
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p0) {
                     ok = issue_pv(0, it);
                     if (!ok) break;
-                    if (it == N - 1) tc_commit(bar(B_O_DONE + 0));
+                    if (J - it == jlo[0]) tc_commit(bar(B_O_DONE + 0));  // its last tile
                     if (!p1) tc_commit(bar(B_V_EMPTY + it % C::VST));
                 }
             }
@@ -297,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp >> 2;          // sub-tile
         const bool my_act = t ? act[1] : act[0];
         const int my_jhi = t ? jhi[1] : jhi[0];
+        const int my_jlo = t ? jlo[1] : jlo[0];
+        const int r_first = row0 + t * C::BM, r_last = r_first + C::BM - 1;
         const int row = threadIdx.x & 127;  // row in the sub-tile == TMEM lane
         const int row_g = row0 + t * C::BM + row;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -307,7 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_run = 0.f;         // sum of P over the keys seen, relative to m_used
         bool ok = true;
         if (my_act) {
-            const int n_t = my_jhi + 1;
+            const int n_t = my_jhi - my_jlo + 1;
+            // allowed keys of this row: [k_lo, k_hi)
+            const int k_lo = (p.wl >= 0) ? row_g - p.wl : 0;
+            const int k_hi = (p.wr >= 0) ? min(p.Sk, row_g + p.wr + 1) : p.Sk;
             for (int i = 0; i < n_t; ++i) {
                 ok = wait(B_S_FULL + t, (uint32_t)i & 1u);
                 ok = __all_sync(0xffffffffu, ok);
@@ -318,16 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-                if (i == 0 && mask_first) {
-                    // keys allowed for this row in this tile: columns [0, lim)
-                    const int end = p.causal ? min(p.Sk, row_g + 1) : p.Sk;
-                    const int lim = end - my_jhi * C::BN;
+                // A tile needs the mask unless every row of the sub-tile may see all
+                // of its keys (causal: only the diagonal tile; ragged: the last).
+                const int col0 = (my_jhi - i) * C::BN;
+                const bool masked = col0 + C::BN > p.Sk || (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
+                                    (p.wl >= 0 && col0 < r_last - p.wl);
+                const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
+                auto apply_mask = [&]() {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
-                }
+                            if (c * 32 + e < lim_lo || c * 32 + e >= lim_hi) s[c][e] = __float_as_uint(-INFINITY);
+                };
+                if (masked) apply_mask();
                 // P is computed against the max already in use.  The row max is
                 // only taken on the first tile, or again for a tile whose sum shows
                 // a score more than 2^64 above that max (the sum also catches inf
@@ -348,13 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
                                               __uint_as_float(s[c][e + 2 * q + 1]));
                     const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
-                    alpha = ex2_approx(m_used - m_new);  // 0 on the first tile
+                    // 0 on a row's first keys; 1 while a row has seen no allowed key
+                    alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
                     m_used = m_new;
                 };
                 auto exp_pass = [&]() {
                     // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
                     // row sum in four packed partial sums
-                    const uint64_t nm2 = f2_pack(-m_used, -m_used);
+                    const float nm = (m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
+                    const uint64_t nm2 = f2_pack(nm, nm);
                     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -374,14 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
                     sum = (a0 + a1) + (b0 + b1);
                 };
-                if (i == 0) take_max();
+                // the max is taken while any row of the warp has no allowed key
+                // yet (always on the first tile)
+                const bool took_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+                if (took_max) take_max();
                 exp_pass();
-                const bool redo = i > 0 && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
+                const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
                 if (redo) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                    if (masked) apply_mask();
                     take_max();
                     exp_pass();
                 }
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
                 tmem_st_wait64(pk);
                 l_run = l_run * alpha + sum;
-                if (redo) {
+                if (redo || (took_max && i > 0)) {
                     // O holds the earlier tiles relative to the old max: rescale it
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {

@@ -17,7 +17,8 @@ struct FwdParams {
     int Sq, Sk;
     int n_mblk;        // ceil(Sq / kCtaRows)
     int n_kv;          // ceil(Sk / kBlockN)
-    int causal;
+    int causal;        // longest-first query-block order (triangular work)
+    int wl, wr;        // key j allowed for query i iff i-wl <= j <= i+wr; -1 = unbounded
     float scale_log2;  // scale * log2(e)
     unsigned long long timeout_ns;  // bound of every on-chip wait
 };

@@ -33,6 +33,12 @@ class Workload:
     D: int
     causal: bool
     q_mult: float = 1.0
+    window_left: int = -1   # keys i - window_left .. i (+ window_right); -1: unbounded
+
+    @property
+    def window(self):
+        """(wl, wr) of the key band: causal is (-1, 0), full attention (-1, -1)."""
+        return (self.window_left, 0 if self.causal else -1)
 
     @property
     def scale(self) -> float:
@@ -40,24 +46,34 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Matmul FLOPs 4*B*H*Sq*Sk*D, halved when causal (the metric's rule)."""
+        """Matmul FLOPs 4*B*H*Sq*Sk*D, halved when causal (the metric's rule); with a
+        bounded window, 4*B*H*D times the exact number of allowed (query, key) pairs."""
+        if self.window_left >= 0:
+            i = np.arange(self.Sq)
+            hi = np.minimum(self.Sk - 1, i if self.causal else self.Sk - 1)
+            lo = np.maximum(0, i - self.window_left)
+            return 4.0 * self.B * self.H * self.D * float(np.maximum(hi - lo + 1, 0).sum())
         f = 4.0 * self.B * self.H * self.Sq * self.Sk * self.D
         return f / 2 if self.causal else f
 
     def describe(self) -> str:
         c = "causal" if self.causal else "non-causal"
+        if self.window_left >= 0:
+            c += f", sliding window of {self.window_left + 1} keys"
         extra = f", Q x{self.q_mult:g}" if self.q_mult != 1.0 else ""
         return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, bf16 N(0,1)"
                 f"{extra}, scale=1/sqrt({self.D}), {c}")
 
 
-# The five attention-forward workloads, in order (index = seed offset).
+# The attention-forward workloads, in order (index = seed offset).
 WORKLOADS = [
     Workload("b1h1s128d64", 1, 1, 128, 128, 64, False),
     Workload("b8h16s2048d128", 8, 16, 2048, 2048, 128, False),
     Workload("b4h16s4096d128_causal", 4, 16, 4096, 4096, 128, True),
     Workload("b1h16s16384d128_causal", 1, 16, 16384, 16384, 128, True),
     Workload("b16h32s1000d64_causal_q4", 16, 32, 1000, 1000, 64, True, 4.0),
+    # sliding-window causal attention (4096-key window), long sequence
+    Workload("b2h32s16384d128_swa4096", 2, 32, 16384, 16384, 128, True, 1.0, 4095),
 ]
 
 

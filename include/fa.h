@@ -79,6 +79,26 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
            int Sq, int Sk, int D, float scale, int causal, void *stream);
 
 /*
+ * fa_fwd_window -- attention forward restricted to a band of keys around each
+ * query: key j is allowed for query i iff  i - window_left <= j <= i + window_right.
+ * A bound of -1 means unbounded on that side; window_right = 0 is causal, and
+ * (window_left = W, window_right = 0) is causal sliding-window attention.
+ * This is the sliding-window generalisation of causal block skipping named in
+ * "FlashAttention-2 — L3 Cross-Paper Synthesis", §5 item 4: key tiles outside
+ * every row's band are skipped whole, tiles crossing a band edge are masked.
+ *
+ * Arguments, layout, ownership and outputs are those of fa_fwd (O and LSE
+ * over the allowed keys only).  A bounded window (either bound >= 0) needs
+ * Sq == Sk, so every query row sees at least its own key.
+ * Errors: those of fa_fwd, plus FA_ERR_BAD_WINDOW for a bound below -1 or a
+ * bounded window with Sq != Sk.  fa_fwd(..., causal, ...) equals
+ * fa_fwd_window(..., -1, causal ? 0 : -1, ...).
+ */
+int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                  int Sq, int Sk, int D, float scale, int window_left, int window_right,
+                  void *stream);
+
+/*
  * fa_strerror -- static English text for a status code.  For FA_ERR_CUDA
  * the text of the most recent CUDA error seen by this thread is appended.
  * The returned pointer stays valid until the next call on the same thread.

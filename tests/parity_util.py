@@ -19,10 +19,14 @@ TOL_O_MEAN = 2e-3
 TOL_LSE = 1e-3
 
 
-def run_gpu(q, k, v, scale, causal, stream=None):
-    """q, k, v: CPU bf16 tensors.  Returns (O float64 numpy, LSE float64 numpy)."""
+def run_gpu(q, k, v, scale, causal, stream=None, window=None):
+    """q, k, v: CPU bf16 tensors.  Returns (O float64 numpy, LSE float64 numpy).
+    With `window` = (wl, wr) the banded entry point is used instead."""
     dq, dk, dv = (t.cuda() for t in (q, k, v))
-    o, lse = fa.fa_fwd(dq, dk, dv, scale=scale, causal=causal, stream=stream)
+    if window is None:
+        o, lse = fa.fa_fwd(dq, dk, dv, scale=scale, causal=causal, stream=stream)
+    else:
+        o, lse = fa.fa_fwd_window(dq, dk, dv, window[0], window[1], scale=scale, stream=stream)
     torch.cuda.synchronize()
     return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
 

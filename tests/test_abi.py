@@ -110,3 +110,17 @@ def test_torch_wrapper_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, o=q.clone(), lse=torch.zeros(1, 1, 128), stream=0)
+
+
+def wcall(wl, wr, Sq=128, Sk=128, **kw):
+    return fa.fa_fwd_window_raw(A, A2, A3, A4, A5, 1, 1, Sq, Sk, 64, 0.125, wl, wr, 0)
+
+
+def test_window_argument_checks():
+    assert wcall(-2, 0) == fa.FA_ERR_BAD_WINDOW
+    assert wcall(5, -3) == fa.FA_ERR_BAD_WINDOW
+    assert wcall(16, 0, Sq=128, Sk=256) == fa.FA_ERR_BAD_WINDOW
+    assert fa.fa_fwd_window_raw(0, A2, A3, A4, A5, 1, 1, 128, 128, 64, 0.125, 4, 0, 0) == \
+        fa.FA_ERR_NULLPTR
+    assert fa.fa_fwd_window_raw(A, A2, A3, A4, A5, 1, 1, 128, 128, 96, 0.125, 4, 0, 0) == \
+        fa.FA_ERR_UNSUPPORTED_D

@@ -68,14 +68,15 @@ def test_parity_other_scale():
 def test_parity_workload(index):
     w = WORKLOADS[index]
     q, k, v = workload_qkv(index)
-    og, lg = run_gpu(q, k, v, w.scale, w.causal)
+    win = w.window if w.window_left >= 0 else None
+    og, lg = run_gpu(q, k, v, w.scale, w.causal, window=win)
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     if w.B * w.H * w.Sq <= 4096:
-        orf, lrf = oracle.attn_fwd(qb, kb, vb, w.scale, w.causal)
+        orf, lrf = oracle.attn_fwd(qb, kb, vb, w.scale, w.causal, w.window)
         compare(og, lg, orf, lrf, w.name)
         return
     bh, rows = sample_rows(w.B, w.H, w.Sq, n_random=160, seed=index)
-    orf, lrf = oracle.attn_fwd_rows(qb, kb, vb, bh, rows, w.scale, w.causal)
+    orf, lrf = oracle.attn_fwd_rows(qb, kb, vb, bh, rows, w.scale, w.causal, w.window)
     og2 = og.reshape(w.B * w.H, w.Sq, w.D)[bh, rows]
     lg2 = lg.reshape(w.B * w.H, w.Sq)[bh, rows]
     compare(og2, lg2, orf, lrf, w.name + " (sampled rows)")
