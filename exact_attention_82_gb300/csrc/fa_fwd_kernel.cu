@@ -99,12 +99,15 @@ constexpr uint32_t SLOT_ABORT = 204;  // byte offset of the abort flag
 constexpr unsigned long long kDrainNs = 20ull * 1000 * 1000;  // 20 ms
 constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+2 idle)
 // Register split.  At launch every thread has 168 (3 warps per SM sub-partition);
-// the MMA/TMA warpgroup drops to 56 and the softmax warpgroups rise to 224:
-// 256 x 224 + 128 x 56 = 64512 = 384 x 168, the block's launch total.
-constexpr uint32_t kRegsSoftmax = 224, kRegsOther = 56;
+// the MMA/TMA warpgroup drops to 72 and the softmax warpgroups rise to 216:
+// 256 x 216 + 128 x 72 = 64512 = 384 x 168, the block's launch total.
+constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 72;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
 
-template <int D>
+// WIN: a bounded key band (window_left >= 0 or window_right > 0).  Without it
+// (full or causal attention) only a sub-tile's first key tile can need a mask
+// and every row has an allowed key in it, which the code below exploits.
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         act[t] = r_first < p.Sq;
         jhi[t] = p.n_kv - 1;
         if (p.wr >= 0) jhi[t] = min(jhi[t], (r_last + p.wr) / C::BN);
-        jlo[t] = (p.wl >= 0) ? max(0, (r_first - p.wl) / C::BN) : 0;
+        jlo[t] = (WIN && p.wl >= 0) ? max(0, (r_first - p.wl) / C::BN) : 0;
     }
     const int J = act[1] ? max(jhi[0], jhi[1]) : jhi[0];  // first key tile of the CTA
     const int J_lo = jlo[0];                              // sub-tile 0 reaches lowest
@@ -233,62 +236,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ======================================================= MMA issuer
         regs_decrease<kRegsOther>();
         if (lane == 0) {
+            // This thread is on the critical path of every tile, so its loop is
+            // kept lean: descriptors are a 64-bit base plus compile-time offsets
+            // (the start-address field cannot carry: shared addresses < 256 KB),
+            // ring stages and phases advance incrementally, and participation is
+            // a precomputed iteration range per sub-tile.
+            const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
+            const uint64_t dq1 = sw128_desc(sQ + C::QT_BYTES, 16, 1024);
+            const uint64_t dk = sw128_desc(sK, 16, 1024);
+            const uint64_t dv = sw128_desc(sV, C::CHUNK, 1024);
+            const int first0 = J - jhi[0], last0 = J - jlo[0];
+            const int first1 = act[1] ? J - jhi[1] : N, last1 = act[1] ? J - jlo[1] : -1;
             bool ok = wait(B_Q_FULL, 0);
-            int npv[2] = {0, 0};  // P V products issued per sub-tile
-            auto part = [&](int t, int it) { return act[t] && (J - it) <= jhi[t] && (J - it) >= jlo[t]; };
-            auto issue_s = [&](int t, int sk) {
-                const uint32_t qb = sQ + t * C::QT_BYTES;
-                const uint32_t kb = sK + sk * C::KV_BYTES;
+            int npv0 = 0, npv1 = 0;        // P V products issued per sub-tile
+            int sk = 0, sv = 0, svp = 0;   // K stage; V stage of the current and previous tile
+            uint32_t kph = 0, vph = 0, vpph = 0;
+            auto issue_s = [&](uint64_t dq, uint32_t s_tm) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                    tc_mma_ss(tmem + t * 128, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                              C::IDESC_S, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(B_S_FULL + t));
             };
-            auto issue_pv = [&](int t, int it) -> bool {
-                const int sv = it % C::VST;
-                if (!wait(B_P_FULL + t, (uint32_t)npv[t] & 1u)) return false;
-                if (!wait(B_V_FULL + sv, (uint32_t)(it / C::VST) & 1u)) return false;
+            auto issue_pv = [&](int t, int npv, int stage, uint32_t phase) -> bool {
+                if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                if (!wait(B_V_FULL + stage, phase)) return false;
                 tc_fence_after();
-                const uint32_t vb = sV + sv * C::KV_BYTES;
+                const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
                     // A = P_t in TMEM (8 columns = 16 keys per step); B = V, MN-major
-                    tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8,
-                              sw128_desc(vb + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
-                              (npv[t] > 0 || kk > 0) ? 1u : 0u);
-                ++npv[t];
+                    tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * 2048) >> 4),
+                              C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
             for (int it = 0; ok && it < N; ++it) {
-                const int sk = it % C::KST;
-                ok = wait(B_K_FULL + sk, (uint32_t)(it / C::KST) & 1u);
+                ok = wait(B_K_FULL + sk, kph);
                 if (!ok) break;
                 tc_fence_after();
-                const bool p0 = part(0, it), p1 = part(1, it);
-                if (p0) issue_s(0, sk);
-                if (it > 0 && part(1, it - 1)) {
-                    ok = issue_pv(1, it - 1);
-                    if (!ok) break;
-                    if (J - (it - 1) == jlo[1]) tc_commit(bar(B_O_DONE + 1));  // its last tile
-                    tc_commit(bar(B_V_EMPTY + (it - 1) % C::VST));
+                const bool p0 = it >= first0 && it <= last0;
+                const bool p1 = it >= first1 && it <= last1;
+                if (p0) {
+                    issue_s(dq0, tmem);
+                    tc_commit(bar(B_S_FULL + 0));
                 }
-                if (p1) issue_s(1, sk);
+                if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
+                    ok = issue_pv(1, npv1++, svp, vpph);
+                    if (!ok) break;
+                    if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                    tc_commit(bar(B_V_EMPTY + svp));
+                }
+                if (p1) {
+                    issue_s(dq1, tmem + 128);
+                    tc_commit(bar(B_S_FULL + 1));
+                }
                 tc_commit(bar(B_K_EMPTY + sk));
                 if (p0) {
-                    ok = issue_pv(0, it);
+                    ok = issue_pv(0, npv0++, sv, vph);
                     if (!ok) break;
-                    if (J - it == jlo[0]) tc_commit(bar(B_O_DONE + 0));  // its last tile
-                    if (!p1) tc_commit(bar(B_V_EMPTY + it % C::VST));
+                    if (it == last0) tc_commit(bar(B_O_DONE + 0));
+                    if (!p1) tc_commit(bar(B_V_EMPTY + sv));
                 }
+                if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                svp = sv;
+                vpph = vph;
+                if (++sv == C::VST) { sv = 0; vph ^= 1u; }
             }
-            if (ok && part(1, N - 1)) {
-                ok = issue_pv(1, N - 1);
+            if (ok && last1 == N - 1) {
+                ok = issue_pv(1, npv1, svp, vpph);
                 if (ok) {
                     tc_commit(bar(B_O_DONE + 1));
-                    tc_commit(bar(B_V_EMPTY + (N - 1) % C::VST));
+                    tc_commit(bar(B_V_EMPTY + svp));
                 }
             }
             // wind down: every MMA issued here is complete before TMEM is freed
@@ -330,8 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A tile needs the mask unless every row of the sub-tile may see all
                 // of its keys (causal: only the diagonal tile; ragged: the last).
                 const int col0 = (my_jhi - i) * C::BN;
-                const bool masked = col0 + C::BN > p.Sk || (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
-                                    (p.wl >= 0 && col0 < r_last - p.wl);
+                const bool masked = WIN ? (col0 + C::BN > p.Sk || (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
+                                           (p.wl >= 0 && col0 < r_last - p.wl))
+                                        : (i == 0 && (p.wr >= 0 || (p.Sk % C::BN) != 0));
                 const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
                 auto apply_mask = [&]() {
 #pragma unroll
@@ -362,13 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               __uint_as_float(s[c][e + 2 * q + 1]));
                     const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
                     // 0 on a row's first keys; 1 while a row has seen no allowed key
-                    alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+                    alpha = (WIN && m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
                     m_used = m_new;
                 };
                 auto exp_pass = [&]() {
                     // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
                     // row sum in four packed partial sums
-                    const float nm = (m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
+                    const float nm = (WIN && m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
                     const uint64_t nm2 = f2_pack(nm, nm);
                     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
@@ -391,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 // the max is taken while any row of the warp has no allowed key
                 // yet (always on the first tile)
-                const bool took_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+                const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
                 if (took_max) take_max();
                 exp_pass();
                 const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
                 tmem_st_wait64(pk);
                 l_run = l_run * alpha + sum;
-                if (redo || (took_max && i > 0)) {
+                if (redo || (WIN && took_max && i > 0)) {
                     // O holds the earlier tiles relative to the old max: rescale it
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -499,22 +518,26 @@ int fwd_smem_bytes(int D) {
     return D == 64 ? (int)FwdCfg<64>::SMEM : (int)FwdCfg<128>::SMEM;
 }
 
-template <int D>
+template <int D, bool WIN>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas,
                                 cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_sm103a<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FwdCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    fa_fwd_sm103a<D><<<dim3((unsigned)n_ctas), dim3(kThreads), FwdCfg<D>::SMEM, stream>>>(tm_q, tm_k, tm_v,
-                                                                                        tm_o, p);
+    fa_fwd_sm103a<D, WIN><<<dim3((unsigned)n_ctas), dim3(kThreads), FwdCfg<D>::SMEM, stream>>>(tm_q, tm_k,
+                                                                                             tm_v, tm_o, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream) {
-    if (D == 64) return launch_fwd_d<64>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    return launch_fwd_d<128>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    const bool win = p.wl >= 0 || p.wr > 0;
+    if (D == 64)
+        return win ? launch_fwd_d<64, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+                   : launch_fwd_d<64, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    return win ? launch_fwd_d<128, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+               : launch_fwd_d<128, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
 }
 
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream) {
