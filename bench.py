@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fwd attention TFLOP/s & % of GB300 dense BF16 peak (causal FLOPs halved)"
 FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["exact_attention_82_gb300/csrc/fa_fwd_kernel.cu",
                   "exact_attention_82_gb300/csrc/sm103_ptx.cuh",
@@ -160,6 +161,17 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- our arm
+def run_path(fa, w, q, k, v, o, lse, ws, stream):
+    """One step of workload `w` through the library's public call for its path."""
+    if w.path == "splitkv":
+        fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, scale=w.scale, workspace=ws, stream=stream)
+    elif w.window_left >= 0:
+        fa.fa_fwd_window(q, k, v, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
+                         stream=stream)
+    else:
+        fa.fa_fwd(q, k, v, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -177,12 +189,13 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    ws = None
+    if w.path == "splitkv":
+        ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
+                         dtype=torch.uint8, device=dev)
+
     def step():
-        if w.window_left >= 0:
-            fa.fa_fwd_window(dq, dk, dv, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
-                             stream=stream)
-        else:
-            fa.fa_fwd(dq, dk, dv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+        run_path(fa, w, dq, dk, dv, o, lse, ws, stream)
 
     def barrier():
         if world > 1:
@@ -226,6 +239,19 @@ def run_ours(args, rank, world, local_rank):
     tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
     value = whole_job_tflops(w.flops, world, ms)
     traffic = traffic_per_launch(w.name)
+    if w.path == "splitkv":
+        # decode reads each key and value once: bound by HBM bandwidth
+        hbm_peak = float(peaks["hbm_gbs"]) if peaks else FALLBACK_HBM_GBS
+        gbs = w.hbm_bytes / (ms_local * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(gbs / hbm_peak, 4),
+                    "peak_source": f"{which}: hbm_gbs (copy bandwidth)" if peaks
+                    else "fallback: 6.8 TB/s", "traffic": traffic}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(tflops_launch / peak, 4),
+                    "peak_source": f"{which}: bf16_tflops (burst, cuBLAS bf16 GEMM)"
+                    if peaks else "fallback: 1.9 PFLOP/s bf16", "traffic": traffic}
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -237,15 +263,10 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed before every step (256 MiB write outside the timed events)",
                    "pct_of_bf16_peak": round(100.0 * tflops_launch / peak, 2),
                    "wall_s_timed_region": round(t_wall, 4)},
-        "roofline": {"bound": "tensor", "achieved": round(tflops_launch, 2),
-                     "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tflops_launch / peak, 4),
-                     "peak_source": f"{which}: bf16_tflops (burst, cuBLAS bf16 GEMM)"
-                     if peaks else "fallback: 1.9 PFLOP/s bf16",
-                     "traffic": traffic},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if w.path == "splitkv" else 1),
         "clocks": clk,
         "impl": "ours",
     }
@@ -265,6 +286,10 @@ def run_e2e(args, w, q, k, v, dev, world):
     dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
     do = torch.empty_like(ho, device=dev)
     dl = torch.empty_like(hl, device=dev)
+    ws = None
+    if w.path == "splitkv":
+        ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
+                         dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 50))
 
@@ -272,11 +297,7 @@ def run_e2e(args, w, q, k, v, dev, world):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        if w.window_left >= 0:
-            fa.fa_fwd_window(dq, dk, dv, w.window[0], w.window[1], o=do, lse=dl, scale=w.scale,
-                             stream=stream)
-        else:
-            fa.fa_fwd(dq, dk, dv, o=do, lse=dl, scale=w.scale, causal=w.causal, stream=stream)
+        run_path(fa, w, dq, dk, dv, do, dl, ws, stream)
         ho.copy_(do, non_blocking=True)
         hl.copy_(dl, non_blocking=True)
 

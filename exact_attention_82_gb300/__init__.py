@@ -18,7 +18,9 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_str
            "fa_selftest_bounded_wait", "fa_version", "FAError", "lib", "library_path",
            "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
-           "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW"]
+           "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
+           "fa_fwd_splitkv", "fa_fwd_splitkv_raw", "fa_fwd_splitkv_workspace_bytes",
+           "fa_splitkv_num_splits"]
 
 FA_OK = 0
 FA_ERR_NULLPTR = -1
@@ -31,6 +33,7 @@ FA_ERR_CUDA = -7
 FA_ERR_TIMEOUT = -8
 FA_ERR_ALIAS = -9
 FA_ERR_BAD_WINDOW = -10
+FA_ERR_WORKSPACE = -11
 
 _lock = threading.Lock()
 _lib = None
@@ -43,6 +46,10 @@ _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
     "fa_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
                            _vp]),
+    "fa_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp,
+                            ctypes.c_size_t, _vp]),
+    "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
+    "fa_splitkv_num_splits": (_i, [_i, _i, _i, _i, _i]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
@@ -161,6 +168,45 @@ def fa_fwd_window(q, k, v, window_left: int, window_right: int, o=None, lse=None
                            _stream_ptr(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_window")
+    return o, lse
+
+
+def fa_fwd_splitkv_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                       H: int, Sq: int, Sk: int, D: int, scale: float, num_splits: int,
+                       ws_ptr: int, ws_bytes: int, stream_ptr: int) -> int:
+    """The split-KV C call with raw device pointers; returns the status code."""
+    return lib().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
+                                int(num_splits), ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, Sq: int, Sk: int, D: int,
+                                   num_splits: int = 0) -> int:
+    return lib().fa_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, D, num_splits)
+
+
+def fa_splitkv_num_splits(B: int, H: int, Sq: int, Sk: int, D: int) -> int:
+    return lib().fa_splitkv_num_splits(B, H, Sq, Sk, D)
+
+
+def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, num_splits: int = 0,
+                   workspace=None, stream=None):
+    """Decode attention (1..8 query rows per head, every key visible) with the keys
+    of each head split across CTAs.  ``workspace`` is a CUDA uint8 tensor of at
+    least fa_fwd_splitkv_workspace_bytes(...) bytes (allocated here if None)."""
+    import torch
+
+    o, lse, B, H, Sq, Sk, D = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = D ** -0.5
+    need = fa_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), B, H, Sq, Sk, D, scale, num_splits,
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv")
     return o, lse
 
 

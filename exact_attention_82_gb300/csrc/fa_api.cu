@@ -11,7 +11,11 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+
+using std::max;
+using std::min;
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -82,6 +86,7 @@ extern "C" const char *fa_strerror(int status) {
         case FA_ERR_TIMEOUT: s = "an on-chip wait gave up (bounded-wait timeout)"; break;
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
         case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1, and a bounded window needs Sq == Sk"; break;
+        case FA_ERR_WORKSPACE: s = "workspace missing, not 16-byte aligned, or smaller than required"; break;
         default: s = "unknown status"; break;
     }
     if (status == FA_ERR_CUDA && t_last_cuda != cudaSuccess)
@@ -159,11 +164,117 @@ extern "C" int fa_fwd_window(const void *q, const void *k, const void *v, void *
     return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream);
 }
 
-extern "C" int fa_device_status(void *stream) {
-    int v = 0;
-    const cudaError_t e = fa::status_read_and_clear(&v, (cudaStream_t)stream);
+// ------------------------------------------------------------- split-KV path
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Keys per split for `splits` ranges: a multiple of the 128-key tile.
+static int split_chunk(int Sk, int splits) {
+    const int per = (Sk + splits - 1) / splits;
+    return ((per + fa::kSplitTileKeys - 1) / fa::kSplitTileKeys) * fa::kSplitTileKeys;
+}
+
+static int resolve_splits(int B, int H, int Sk, int num_splits) {
+    const int max_splits = (Sk + fa::kSplitTileKeys - 1) / fa::kSplitTileKeys;
+    int s = num_splits;
+    if (s <= 0) {
+        // Our heuristic: among split counts keeping >= 256 keys per split (up to
+        // 256 splits), take the one whose CTAs fill the SMs' last wave best,
+        // preferring at least four waves; ties go to fewer splits.
+        const long long bh = (long long)B * H;
+        const int nsm = sm_count();
+        const int cap = max(1, min(256, (Sk + 255) / 256));
+        double best = -1.0;
+        s = 1;
+        for (int c = 1; c <= cap; ++c) {
+            const long long ctas = bh * c;
+            const long long waves = (ctas + nsm - 1) / nsm;
+            double score = (double)ctas / (double)(waves * nsm);
+            if (ctas < 4ll * nsm) score *= (double)ctas / (4.0 * nsm);
+            if (score > best + 1e-9) {
+                best = score;
+                s = c;
+            }
+        }
+    }
+    s = min(s, max_splits);
+    const int chunk = split_chunk(Sk, s);
+    return (Sk + chunk - 1) / chunk;  // no empty split
+}
+
+static size_t splitkv_bytes(long long BH, int Sq, int D, int splits) {
+    const size_t o_bytes = (size_t)BH * splits * Sq * D * sizeof(float);
+    const size_t o_pad = (o_bytes + 255) & ~(size_t)255;
+    return o_pad + (size_t)BH * splits * Sq * sizeof(float);
+}
+
+static bool splitkv_shape_ok(int B, int H, int Sq, int Sk, int D) {
+    return B >= 1 && H >= 1 && Sq >= 1 && Sq <= fa::kSplitMaxSq && Sk >= 1 && (D == 64 || D == 128) &&
+           (long long)B * H <= 65535;
+}
+
+extern "C" int fa_splitkv_num_splits(int B, int H, int Sq, int Sk, int D) {
+    if (!splitkv_shape_ok(B, H, Sq, Sk, D)) return FA_ERR_BAD_SHAPE;
+    return resolve_splits(B, H, Sk, 0);
+}
+
+extern "C" size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Sk, int D, int num_splits) {
+    if (!splitkv_shape_ok(B, H, Sq, Sk, D) || num_splits > 256) return 0;
+    return splitkv_bytes((long long)B * H, Sq, D, resolve_splits(B, H, Sk, num_splits));
+}
+
+extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                              int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (Sq > fa::kSplitMaxSq || (long long)B * H > 65535 || num_splits > 256) return FA_ERR_BAD_SHAPE;
+    const long long BH = (long long)B * H;
+    const int splits = resolve_splits(B, H, Sk, num_splits);
+    const size_t need = splitkv_bytes(BH, Sq, D, splits);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    const size_t kv_bytes = (size_t)BH * Sk * D * 2, q_bytes = (size_t)BH * Sq * D * 2;
+    if (overlaps(workspace, need, q, q_bytes) || overlaps(workspace, need, k, kv_bytes) ||
+        overlaps(workspace, need, v, kv_bytes) || overlaps(workspace, need, o, q_bytes) ||
+        overlaps(workspace, need, lse, (size_t)BH * Sq * 4))
+        return FA_ERR_ALIAS;
+    if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
+    CUtensorMap tm_k, tm_v;
+    if (!encode_bhsd(&tm_k, k, D, Sk, BH, fa::kSplitTileKeys) || !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kSplitTileKeys))
+        return fail_cuda(cudaErrorInvalidValue);
+    fa::SplitParams p;
+    p.q = q;
+    p.o = o;
+    p.lse = lse;
+    p.o_part = static_cast<float *>(workspace);
+    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                           (((size_t)BH * splits * Sq * D * sizeof(float) + 255) & ~(size_t)255));
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.chunk = split_chunk(Sk, splits);
+    p.splits = splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = kWaitLimitNs;
+    const cudaError_t e = fa::launch_splitkv(D, tm_k, tm_v, p, (int)BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
-    return v;
+    return FA_OK;
+}
+
+extern "C" int fa_device_status(void *stream) {
+    int v = 0, w = 0;
+    cudaError_t e = fa::status_read_and_clear(&v, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = fa::splitkv_status_read_and_clear(&w);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return v != FA_OK ? v : w;
 }
 
 extern "C" int fa_selftest_bounded_wait(int timeout_us, void *stream) {

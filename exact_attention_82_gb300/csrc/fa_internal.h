@@ -23,6 +23,26 @@ struct FwdParams {
     unsigned long long timeout_ns;  // bound of every on-chip wait
 };
 
+// Split-KV (decode) launch: partials per (head, split), then a merge.
+constexpr int kSplitMaxSq = 8;     // query rows per head the split path takes
+constexpr int kSplitTileKeys = 64;
+struct SplitParams {
+    const void *q;      // bf16 [B*H, Sq, D]
+    void *o;            // bf16 [B*H, Sq, D]
+    float *lse;         // fp32 [B*H, Sq]
+    float *o_part;      // fp32 [B*H, splits, Sq, D]   (workspace)
+    float *lse_part;    // fp32 [B*H, splits, Sq]      (workspace)
+    int Sq, Sk;
+    int chunk;          // keys per split, a multiple of kSplitTileKeys
+    int splits;         // ceil(Sk / chunk)
+    float scale_log2;
+    unsigned long long timeout_ns;
+};
+int splitkv_smem_bytes(int D);
+cudaError_t launch_splitkv(int D, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p, int BH,
+                           cudaStream_t stream);
+cudaError_t splitkv_status_read_and_clear(int *out);
+
 // Dynamic shared memory the forward kernel for head dim D asks for.
 int fwd_smem_bytes(int D);
 

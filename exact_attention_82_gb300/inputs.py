@@ -34,6 +34,7 @@ class Workload:
     causal: bool
     q_mult: float = 1.0
     window_left: int = -1   # keys i - window_left .. i (+ window_right); -1: unbounded
+    path: str = "fwd"       # "fwd" (query-block parallel) or "splitkv" (decode, key-split)
 
     @property
     def window(self):
@@ -56,10 +57,18 @@ class Workload:
         f = 4.0 * self.B * self.H * self.Sq * self.Sk * self.D
         return f / 2 if self.causal else f
 
+    @property
+    def hbm_bytes(self) -> float:
+        """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
+        return float(self.B * self.H * (2 * (self.Sq + 2 * self.Sk) * self.D + 2 * self.Sq * self.D
+                                        + 4 * self.Sq))
+
     def describe(self) -> str:
         c = "causal" if self.causal else "non-causal"
         if self.window_left >= 0:
             c += f", sliding window of {self.window_left + 1} keys"
+        if self.path == "splitkv":
+            c += ", split-KV decode"
         extra = f", Q x{self.q_mult:g}" if self.q_mult != 1.0 else ""
         return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, bf16 N(0,1)"
                 f"{extra}, scale=1/sqrt({self.D}), {c}")
@@ -74,6 +83,8 @@ WORKLOADS = [
     Workload("b16h32s1000d64_causal_q4", 16, 32, 1000, 1000, 64, True, 4.0),
     # sliding-window causal attention (4096-key window), long sequence
     Workload("b2h32s16384d128_swa4096", 2, 32, 16384, 16384, 128, True, 1.0, 4095),
+    # decode: one query row per head against a 16384-key cache (HBM-bound)
+    Workload("b8h32q1s16384d128_decode", 8, 32, 1, 16384, 128, False, path="splitkv"),
 ]
 
 

@@ -34,6 +34,8 @@
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -49,7 +51,8 @@ typedef enum {
     FA_ERR_CUDA = -7,               /* CUDA runtime / driver error                   */
     FA_ERR_TIMEOUT = -8,            /* a bounded on-chip wait gave up (status word)  */
     FA_ERR_ALIAS = -9,              /* an output overlaps an input or the other one */
-    FA_ERR_BAD_WINDOW = -10         /* window bound below -1                         */
+    FA_ERR_BAD_WINDOW = -10,        /* window bound below -1, or band with Sq != Sk  */
+    FA_ERR_WORKSPACE = -11          /* workspace missing, misaligned or too small    */
 } fa_status;
 
 /*
@@ -97,6 +100,49 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                   int Sq, int Sk, int D, float scale, int window_left, int window_right,
                   void *stream);
+
+/*
+ * fa_fwd_splitkv -- attention for decode: a few query rows per head against a
+ * long key/value sequence, with the keys of each head split across CTAs.
+ * "FlashAttention-2 — L3 Cross-Paper Synthesis", §5 item 5 (decode needs
+ * parallelism over the key/value sequence); the split-and-merge of v1's
+ * num_splits in "FlashAttention-2 相比 FlashAttention-1，到底改了什么", section
+ * "第一处源码差异：launch grid 怎么铺".  Each split s of a head produces
+ * lse_s = ln sum_{j in s} exp(scale q.k_j) and the normalised partial o_s;
+ * the merge is lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+ * Every query row sees every key (no mask).
+ *
+ *   q, k, v, o, lse, B, H, Sk, D, scale, stream: as fa_fwd
+ *   Sq            1 .. 8 query rows per head
+ *   num_splits    key ranges per head, 1 .. 256; <= 0 picks a count from the
+ *                 problem size and the SM count (fa_splitkv_num_splits);
+ *                 each range holds a multiple of 64 keys, so fewer ranges
+ *                 may be used when Sk is short
+ *   workspace     caller-owned DEVICE scratch of at least
+ *                 fa_fwd_splitkv_workspace_bytes(...) bytes, 16-byte aligned,
+ *                 not overlapping any other argument; it holds fp32 partial
+ *                 results between the two kernels this call enqueues, and
+ *                 must not be used by another call until the stream has run
+ *                 past this one
+ *   B * H         at most 65535
+ *
+ * Errors: those of fa_fwd (causal does not apply), FA_ERR_BAD_SHAPE for
+ * Sq > 8, B*H > 65535 or num_splits > 256, FA_ERR_WORKSPACE for a missing,
+ * misaligned or short workspace.  Deterministic; no atomics.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * fa_fwd_splitkv_workspace_bytes -- bytes of workspace fa_fwd_splitkv needs for
+ * these sizes and num_splits (<= 0: the automatic count); 0 for unsupported sizes.
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Sk, int D, int num_splits);
+
+/* fa_splitkv_num_splits -- the split count fa_fwd_splitkv picks automatically
+ * for these sizes on the current device (or FA_ERR_BAD_SHAPE). */
+int fa_splitkv_num_splits(int B, int H, int Sq, int Sk, int D);
 
 /*
  * fa_strerror -- static English text for a status code.  For FA_ERR_CUDA

@@ -19,11 +19,14 @@ TOL_O_MEAN = 2e-3
 TOL_LSE = 1e-3
 
 
-def run_gpu(q, k, v, scale, causal, stream=None, window=None):
+def run_gpu(q, k, v, scale, causal, stream=None, window=None, splits=None):
     """q, k, v: CPU bf16 tensors.  Returns (O float64 numpy, LSE float64 numpy).
-    With `window` = (wl, wr) the banded entry point is used instead."""
+    With `window` = (wl, wr) the banded entry point is used; with `splits` (an
+    int, 0 = automatic) the split-KV decode entry point."""
     dq, dk, dv = (t.cuda() for t in (q, k, v))
-    if window is None:
+    if splits is not None:
+        o, lse = fa.fa_fwd_splitkv(dq, dk, dv, scale=scale, num_splits=splits, stream=stream)
+    elif window is None:
         o, lse = fa.fa_fwd(dq, dk, dv, scale=scale, causal=causal, stream=stream)
     else:
         o, lse = fa.fa_fwd_window(dq, dk, dv, window[0], window[1], scale=scale, stream=stream)

@@ -49,7 +49,7 @@ def test_library_is_in_tree():
 
 def test_version_and_strerror():
     assert fa.fa_version() >= 100
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         s = fa.fa_strerror(code)
         assert s and s != "unknown status", code
     assert fa.fa_strerror(12345) == "unknown status"
@@ -124,3 +124,24 @@ def test_window_argument_checks():
         fa.FA_ERR_NULLPTR
     assert fa.fa_fwd_window_raw(A, A2, A3, A4, A5, 1, 1, 128, 128, 96, 0.125, 4, 0, 0) == \
         fa.FA_ERR_UNSUPPORTED_D
+
+
+def test_splitkv_sizes_and_checks():
+    n = fa.fa_splitkv_num_splits(8, 32, 1, 16384, 128)
+    assert 1 <= n <= 256
+    need = fa.fa_fwd_splitkv_workspace_bytes(8, 32, 1, 16384, 128, 4)
+    assert need >= 8 * 32 * 4 * 1 * (128 + 1) * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 9, 100, 128, 0) == 0   # Sq > 8
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 100, 96, 0) == 0    # D
+    W = 1 << 42
+
+    def scall(Sq=1, Sk=4096, D=128, splits=0, ws=W, ws_bytes=1 << 30):
+        return fa.fa_fwd_splitkv_raw(A, A2, A3, A4, A5, 1, 1, Sq, Sk, D, 0.1, splits, ws,
+                                     ws_bytes, 0)
+
+    assert scall(Sq=9) == fa.FA_ERR_BAD_SHAPE
+    assert scall(splits=300) == fa.FA_ERR_BAD_SHAPE
+    assert scall(ws=0) == fa.FA_ERR_WORKSPACE
+    assert scall(ws=W + 8) == fa.FA_ERR_WORKSPACE
+    assert scall(ws_bytes=16) == fa.FA_ERR_WORKSPACE
+    assert scall(ws=A + 64) == fa.FA_ERR_ALIAS
