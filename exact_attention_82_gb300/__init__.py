@@ -20,7 +20,7 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_str
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
            "fa_fwd_splitkv", "fa_fwd_splitkv_raw", "fa_fwd_splitkv_workspace_bytes",
-           "fa_splitkv_num_splits"]
+           "fa_splitkv_num_splits", "FA_ERR_SCRATCH_LIMIT"]
 
 FA_OK = 0
 FA_ERR_NULLPTR = -1
@@ -34,6 +34,7 @@ FA_ERR_TIMEOUT = -8
 FA_ERR_ALIAS = -9
 FA_ERR_BAD_WINDOW = -10
 FA_ERR_WORKSPACE = -11
+FA_ERR_SCRATCH_LIMIT = -12
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +50,8 @@ _SIGNATURES = {
     "fa_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp,
                             ctypes.c_size_t, _vp]),
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
+    "fa_fwd_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float,
+                                    _i, _vp]),
     "fa_splitkv_num_splits": (_i, [_i, _i, _i, _i, _i]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),

@@ -87,6 +87,10 @@ extern "C" const char *fa_strerror(int status) {
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
         case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1, and a bounded window needs Sq == Sk"; break;
         case FA_ERR_WORKSPACE: s = "workspace missing, not 16-byte aligned, or smaller than required"; break;
+        case FA_ERR_SCRATCH_LIMIT:
+            s = "needs more scratch than the built-in 16 MiB buffer of fa_fwd_splitkv_noalloc holds; "
+                "pass a workspace to fa_fwd_splitkv instead";
+            break;
         default: s = "unknown status"; break;
     }
     if (status == FA_ERR_CUDA && t_last_cuda != cudaSuccess)
@@ -267,6 +271,21 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
     const cudaError_t e = fa::launch_splitkv(D, tm_k, tm_v, p, (int)BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
+}
+
+extern "C" int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                      int H, int Sq, int Sk, int D, float scale, int num_splits, void *stream) {
+    // Same checks as fa_fwd_splitkv, then the size limit, before any CUDA call.
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (Sq > fa::kSplitMaxSq || (long long)B * H > 65535 || num_splits > 256) return FA_ERR_BAD_SHAPE;
+    const size_t need = splitkv_bytes((long long)B * H, Sq, D, resolve_splits(B, H, Sk, num_splits));
+    if (need > fa::kNoAllocScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    const cudaError_t e = fa::splitkv_scratch(&scratch);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return fa_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, num_splits, scratch, fa::kNoAllocScratchBytes,
+                          stream);
 }
 
 extern "C" int fa_device_status(void *stream) {

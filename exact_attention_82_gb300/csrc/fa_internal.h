@@ -42,6 +42,10 @@ int splitkv_smem_bytes(int D);
 cudaError_t launch_splitkv(int D, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p, int BH,
                            cudaStream_t stream);
 cudaError_t splitkv_status_read_and_clear(int *out);
+// Built-in scratch of fa_fwd_splitkv_noalloc: size, and its device address
+// on the current device (looked up on the first call per device).
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
+cudaError_t splitkv_scratch(void **out);
 
 // Dynamic shared memory the forward kernel for head dim D asks for.
 int fwd_smem_bytes(int D);

@@ -27,6 +27,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -313,6 +315,35 @@ cudaError_t launch_splitkv(int D, const CUtensorMap &tm_k, const CUtensorMap &tm
     else
         fa_splitkv_combine<128><<<dim3(p.Sq, BH), dim3(128), 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------- built-in scratch buffer
+// Scratch for callers that cannot allocate device memory themselves (see
+// fa_fwd_splitkv_noalloc in fa.h).  It lives in the library's own device
+// image: every GPU that loads the library holds these bytes until the
+// process exits, and every call on a device shares them.
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array for the current device.  The first
+// call on a device looks it up (cudaGetSymbolAddress, with that device
+// current) and caches it; later calls only read the cache.  In host code the
+// array's name is just a host-side stand-in, never a device address.
+cudaError_t splitkv_scratch(void **out) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t splitkv_status_read_and_clear(int *out) {

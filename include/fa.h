@@ -52,7 +52,8 @@ typedef enum {
     FA_ERR_TIMEOUT = -8,            /* a bounded on-chip wait gave up (status word)  */
     FA_ERR_ALIAS = -9,              /* an output overlaps an input or the other one */
     FA_ERR_BAD_WINDOW = -10,        /* window bound below -1, or band with Sq != Sk  */
-    FA_ERR_WORKSPACE = -11          /* workspace missing, misaligned or too small    */
+    FA_ERR_WORKSPACE = -11,         /* workspace missing, misaligned or too small    */
+    FA_ERR_SCRATCH_LIMIT = -12      /* more scratch than the built-in buffer holds   */
 } fa_status;
 
 /*
@@ -143,6 +144,31 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Sk, int D, int n
 /* fa_splitkv_num_splits -- the split count fa_fwd_splitkv picks automatically
  * for these sizes on the current device (or FA_ERR_BAD_SHAPE). */
 int fa_splitkv_num_splits(int B, int H, int Sq, int Sk, int D);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call: it exists for
+ * callers such as a process whose device memory is all reserved up front by
+ * another allocator (a cudaMalloc there fails or fragments that pool), or a
+ * latency-critical path that must not take the implicit synchronisation and
+ * driver locks that cudaMalloc/cudaFree can take.  It allocates nothing: the
+ * scratch lives in a 16 MiB array inside this library's device image (every
+ * GPU that loads the library holds it until the process exits).
+ *
+ * Arguments and results are those of fa_fwd_splitkv without the workspace;
+ * the caller still provides q, k, v, o and lse.  The first call on a device
+ * looks up the array's device address for that device (cudaGetSymbolAddress)
+ * and caches it, so make that first call before any stream capture.  All
+ * calls on a device share the one array and it keeps the last call's bytes;
+ * nothing in it needs to start at zero (each call writes every partial result
+ * before reading it).  Calls whose kernels overlap on the GPU (two streams,
+ * or two host threads) race on the array: serialise them.
+ * Errors: those of fa_fwd_splitkv, plus FA_ERR_SCRATCH_LIMIT when the sizes
+ * need more than 16 MiB of scratch (fa_fwd_splitkv_workspace_bytes tells the
+ * need; pass a workspace to fa_fwd_splitkv for larger problems).
+ */
+int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                           int H, int Sq, int Sk, int D, float scale, int num_splits, void *stream);
 
 /*
  * fa_strerror -- static English text for a status code.  For FA_ERR_CUDA

@@ -49,7 +49,7 @@ def test_library_is_in_tree():
 
 def test_version_and_strerror():
     assert fa.fa_version() >= 100
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         s = fa.fa_strerror(code)
         assert s and s != "unknown status", code
     assert fa.fa_strerror(12345) == "unknown status"
@@ -145,3 +145,14 @@ def test_splitkv_sizes_and_checks():
     assert scall(ws=W + 8) == fa.FA_ERR_WORKSPACE
     assert scall(ws_bytes=16) == fa.FA_ERR_WORKSPACE
     assert scall(ws=A + 64) == fa.FA_ERR_ALIAS
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    """64 heads x 8 rows x 256 splits of fp32 partials need ~68 MB > 16 MiB; the
+    call refuses before touching the GPU (pointers here are never used)."""
+    big = [1 << 36, 1 << 38, 1 << 40, 1 << 42, 1 << 44]
+    st = fa.lib().fa_fwd_splitkv_noalloc(*big, 1, 64, 8, 16384, 128, 0.1, 256, 0)
+    assert st == fa.FA_ERR_SCRATCH_LIMIT
+    assert "16 MiB" in fa.fa_strerror(st)
+    assert fa.lib().fa_fwd_splitkv_noalloc(0, *big[1:], 1, 1, 1, 64, 128, 0.1, 0, 0) == \
+        fa.FA_ERR_NULLPTR
