@@ -64,8 +64,11 @@ def _bind(path: str):
     lib.oracle_attn_fwd_bf16.argtypes = [dp] * 5 + common + [ctypes.c_int]
     lib.oracle_attn_fwd_rows_bf16.argtypes = [dp] * 5 + [L, dp, dp] + common + [ctypes.c_int]
     lib.oracle_attn_fwd_tiled_f64.argtypes = [dp] * 5 + common + [L, L]
+    lib.oracle_attn_bwd_f64.argtypes = [dp] * 7 + common + [ctypes.c_int]
+    lib.oracle_attn_bwd_bf16.argtypes = [dp] * 7 + common + [ctypes.c_int]
     for f in (lib.oracle_attn_fwd_f64, lib.oracle_attn_fwd_bf16,
-              lib.oracle_attn_fwd_rows_bf16, lib.oracle_attn_fwd_tiled_f64):
+              lib.oracle_attn_fwd_rows_bf16, lib.oracle_attn_fwd_tiled_f64,
+              lib.oracle_attn_bwd_f64, lib.oracle_attn_bwd_bf16):
         f.restype = ctypes.c_int
     return lib
 
@@ -177,3 +180,23 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact widening of uint16 bf16 bit patterns to float64 (for tests)."""
     u32 = np.asarray(bits, np.uint16).astype(np.uint32) << 16
     return u32.view(np.float32).astype(np.float64)
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool = False, window=(-1, -1),
+             nthreads: int | None = None, lib=None):
+    """Gradients (dQ, dK, dV) of the attention forward for output gradient ``dout``
+    ([B,H,Sq,D], same dtype as q: float64 or uint16 bf16 bits), in float64."""
+    lib = lib or load()
+    q, k, v, B, H, Sq, Sk, D = _prep(q, k, v)
+    dout = np.ascontiguousarray(dout)
+    if dout.dtype != q.dtype or dout.shape != q.shape:
+        raise ValueError("dout must match q in dtype and shape")
+    dq = np.empty((B, H, Sq, D), np.float64)
+    dk = np.empty((B, H, Sk, D), np.float64)
+    dv = np.empty((B, H, Sk, D), np.float64)
+    fn = lib.oracle_attn_bwd_bf16 if q.dtype == np.uint16 else lib.oracle_attn_bwd_f64
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Sq, Sk, D,
+            float(scale), int(bool(causal)), int(window[0]), int(window[1]),
+            nthreads or default_threads())
+    _check(st)
+    return dq, dk, dv

@@ -405,3 +405,170 @@ int oracle_attn_fwd_tiled_f64(const double *q, const double *k, const double *v,
     free(l);
     return st;
 }
+
+/* ------------------------------------------------------------------------ */
+/*
+ * Backward pass of the same attention, from the definition (no tiling):
+ * given dO (the gradient of a loss with respect to O), for each (b, h)
+ *   S_ij  = scale q_i.k_j (allowed keys; -inf elsewhere),  P = softmax_j(S)
+ *   O_i   = sum_j P_ij v_j
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   Delta_i = dO_i . O_i
+ *   dS_ij = P_ij (dP_ij - Delta_i)
+ *   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * ("FlashAttention-2 — L3 Cross-Paper Synthesis", §3 item 1 and §5 item 2:
+ * the backward pass and its five matrix products.)  All of S, P, dP and dS
+ * of a head are materialised; one thread per (batch, head).
+ */
+typedef struct {
+    const void *q, *k, *v, *dout;
+    int bf16;
+    double *dq, *dk, *dv;
+    long B, H, Sq, Sk, D;
+    double scale;
+    int causal;
+    long wl, wr;
+    long next;
+    int status;
+    pthread_mutex_t mu;
+} bwd_job_t;
+
+static void *bwd_worker(void *arg) {
+    bwd_job_t *jb = (bwd_job_t *)arg;
+    const long Sq = jb->Sq, Sk = jb->Sk, D = jb->D;
+    double *qb = (double *)malloc(sizeof(double) * (size_t)(Sq * D));
+    double *kb = (double *)malloc(sizeof(double) * (size_t)(Sk * D));
+    double *vb = (double *)malloc(sizeof(double) * (size_t)(Sk * D));
+    double *gb = (double *)malloc(sizeof(double) * (size_t)(Sq * D));
+    double *P = (double *)malloc(sizeof(double) * (size_t)(Sq * Sk));
+    double *dS = (double *)malloc(sizeof(double) * (size_t)(Sq * Sk));
+    double *O = (double *)malloc(sizeof(double) * (size_t)(Sq * D));
+    double *delta = (double *)malloc(sizeof(double) * (size_t)Sq);
+    int st = ORC_OK;
+    if (!qb || !kb || !vb || !gb || !P || !dS || !O || !delta) st = ORC_ERR_NOMEM;
+    while (st == ORC_OK) {
+        pthread_mutex_lock(&jb->mu);
+        const long bh = jb->next++;
+        const int failed = jb->status != ORC_OK;
+        pthread_mutex_unlock(&jb->mu);
+        if (bh >= jb->B * jb->H || failed) break;
+        job_t view;  /* reuse the widening helper */
+        memset(&view, 0, sizeof view);
+        view.bf16 = jb->bf16;
+        view.D = D;
+        const double *Q = slice_f64(&view, jb->q, bh, Sq, qb);
+        const double *K = slice_f64(&view, jb->k, bh, Sk, kb);
+        const double *V = slice_f64(&view, jb->v, bh, Sk, vb);
+        const double *G = slice_f64(&view, jb->dout, bh, Sq, gb);
+        /* S -> P (row softmax over allowed keys), O */
+        for (long i = 0; i < Sq && st == ORC_OK; ++i) {
+            double m = -INFINITY;
+            for (long j = 0; j < Sk; ++j) {
+                double s = -INFINITY;
+                if (key_allowed(i, j, Sk, jb->causal, jb->wl, jb->wr)) {
+                    double dot = 0.0;
+                    for (long d = 0; d < D; ++d) dot += Q[i * D + d] * K[j * D + d];
+                    s = jb->scale * dot;
+                }
+                P[i * Sk + j] = s;
+                if (s > m) m = s;
+            }
+            if (m == -INFINITY) {
+                st = ORC_ERR_EMPTY_ROW;
+                break;
+            }
+            double sum = 0.0;
+            for (long j = 0; j < Sk; ++j) {
+                P[i * Sk + j] = exp(P[i * Sk + j] - m);
+                sum += P[i * Sk + j];
+            }
+            for (long j = 0; j < Sk; ++j) P[i * Sk + j] /= sum;
+            for (long d = 0; d < D; ++d) {
+                double o = 0.0;
+                for (long j = 0; j < Sk; ++j) o += P[i * Sk + j] * V[j * D + d];
+                O[i * D + d] = o;
+            }
+        }
+        if (st != ORC_OK) break;
+        /* Delta, dP -> dS */
+        for (long i = 0; i < Sq; ++i) {
+            double dl = 0.0;
+            for (long d = 0; d < D; ++d) dl += G[i * D + d] * O[i * D + d];
+            delta[i] = dl;
+            for (long j = 0; j < Sk; ++j) {
+                double dp = 0.0;
+                for (long d = 0; d < D; ++d) dp += G[i * D + d] * V[j * D + d];
+                dS[i * Sk + j] = P[i * Sk + j] * (dp - dl);
+            }
+        }
+        double *dq = jb->dq + bh * Sq * D, *dk = jb->dk + bh * Sk * D, *dv = jb->dv + bh * Sk * D;
+        for (long i = 0; i < Sq; ++i)
+            for (long d = 0; d < D; ++d) {
+                double a = 0.0;
+                for (long j = 0; j < Sk; ++j) a += dS[i * Sk + j] * K[j * D + d];
+                dq[i * D + d] = jb->scale * a;
+            }
+        for (long j = 0; j < Sk; ++j)
+            for (long d = 0; d < D; ++d) {
+                double a = 0.0, b = 0.0;
+                for (long i = 0; i < Sq; ++i) {
+                    a += dS[i * Sk + j] * Q[i * D + d];
+                    b += P[i * Sk + j] * G[i * D + d];
+                }
+                dk[j * D + d] = jb->scale * a;
+                dv[j * D + d] = b;
+            }
+    }
+    if (st != ORC_OK) {
+        pthread_mutex_lock(&jb->mu);
+        if (jb->status == ORC_OK) jb->status = st;
+        pthread_mutex_unlock(&jb->mu);
+    }
+    free(qb); free(kb); free(vb); free(gb); free(P); free(dS); free(O); free(delta);
+    return NULL;
+}
+
+static int run_bwd(bwd_job_t *jb, int nthreads) {
+    jb->next = 0;
+    jb->status = ORC_OK;
+    pthread_mutex_init(&jb->mu, NULL);
+    const long n = jb->B * jb->H;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n) nthreads = (int)n;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    if (th)
+        for (; started < nthreads; ++started)
+            if (pthread_create(&th[started], NULL, bwd_worker, jb) != 0) break;
+    if (started == 0) bwd_worker(jb);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&jb->mu);
+    return jb->status;
+}
+
+static int bwd_entry(const void *q, const void *k, const void *v, const void *dout, int bf16, double *dq,
+                     double *dk, double *dv, long B, long H, long Sq, long Sk, long D, double scale,
+                     int causal, long wl, long wr, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || check_shape(B, H, Sq, Sk, D)) return ORC_ERR_ARG;
+    bwd_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v; jb.dout = dout; jb.bf16 = bf16;
+    jb.dq = dq; jb.dk = dk; jb.dv = dv;
+    jb.B = B; jb.H = H; jb.Sq = Sq; jb.Sk = Sk; jb.D = D;
+    jb.scale = scale; jb.causal = causal; jb.wl = wl; jb.wr = wr;
+    return run_bwd(&jb, nthreads);
+}
+
+int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const double *dout, double *dq,
+                        double *dk, double *dv, long B, long H, long Sq, long Sk, long D, double scale,
+                        int causal, long wl, long wr, int nthreads) {
+    return bwd_entry(q, k, v, dout, 0, dq, dk, dv, B, H, Sq, Sk, D, scale, causal, wl, wr, nthreads);
+}
+
+int oracle_attn_bwd_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                         double *dq, double *dk, double *dv, long B, long H, long Sq, long Sk, long D,
+                         double scale, int causal, long wl, long wr, int nthreads) {
+    return bwd_entry(q, k, v, dout, 1, dq, dk, dv, B, H, Sq, Sk, D, scale, causal, wl, wr, nthreads);
+}

@@ -33,6 +33,16 @@ MUTANTS = {
     "bf16_widening": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
 }
 
+# mistakes planted in the backward pass
+BWD_MUTANTS = {
+    "delta_sign": ("dS[i * Sk + j] = P[i * Sk + j] * (dp - dl);", "dS[i * Sk + j] = P[i * Sk + j] * (dp + dl);"),
+    "dq_no_scale": ("dq[i * D + d] = jb->scale * a;", "dq[i * D + d] = a;"),
+    "dk_uses_k": ("a += dS[i * Sk + j] * Q[i * D + d];", "a += dS[i * Sk + j] * K[i * D + d];"),
+    "dv_transposed_p": ("b += P[i * Sk + j] * G[i * D + d];", "b += P[j * Sk + i] * G[i * D + d];"),
+    "delta_uses_v": ("for (long d = 0; d < D; ++d) dl += G[i * D + d] * O[i * D + d];",
+                     "for (long d = 0; d < D; ++d) dl += G[i * D + d] * V[i * D + d];"),
+}
+
 
 def _pins_pass(lib) -> bool:
     """A small battery of the pins; True only if every one holds."""
@@ -81,3 +91,46 @@ def test_planted_mistake_is_caught(name, tmp_path):
                     str(src), "-lm"], check=True)
     lib = oracle.load(out)
     assert not _pins_pass(lib), f"planted mistake {name} was not caught by the pins"
+
+
+def _bwd_pins_pass(lib) -> bool:
+    """Finite differences of the unmutated forward and torch autograd."""
+    from test_oracle_bwd_pins import _loss
+    rng = np.random.default_rng(5)
+    q, k, v, g = (rng.standard_normal((1, 1, 4, 3)) for _ in range(4))
+    try:
+        dq, dk, dv = oracle.attn_bwd(q, k, v, g, 0.8, True, lib=lib)
+    except oracle.OracleError:
+        return False
+    good = oracle.load()
+    h = 1e-5
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            a = {"q": q, "k": k, "v": v}
+            b = dict(a)
+            a[name], b[name] = xp, xm
+            num = (_loss(a["q"], a["k"], a["v"], g, 0.8, True, (-1, -1), good)
+                   - _loss(b["q"], b["k"], b["v"], g, 0.8, True, (-1, -1), good)) / (2 * h)
+            if not abs(num - grad[idx]) <= 1e-8:
+                return False
+    return True
+
+
+def test_unmutated_backward_passes_battery(oracle_lib):
+    assert _bwd_pins_pass(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_planted_backward_mistake_is_caught(name, tmp_path):
+    before, after = BWD_MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(before) == 1, f"mutation anchor for {name} not unique"
+    src = tmp_path / f"mutant_{name}.c"
+    src.write_text(text.replace(before, after))
+    out = str(tmp_path / f"libmutant_{name}.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", out,
+                    str(src), "-lm"], check=True)
+    assert not _bwd_pins_pass(oracle.load(out)), f"planted mistake {name} was not caught"
