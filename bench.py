@@ -162,14 +162,36 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm
 def run_path(fa, w, q, k, v, o, lse, ws, stream):
-    """One step of workload `w` through the library's public call for its path."""
-    if w.path == "splitkv":
+    """One step of workload `w` through the library's public call for its path.
+    For the backward, `ws` holds (forward O, forward LSE, dO, dQ, dK, dV, Delta)."""
+    if w.path == "bwd":
+        fo, flse, dout, dq, dk, dv, delta = ws
+        fa.fa_bwd(q, k, v, fo, flse, dout, dq=dq, dk=dk, dv=dv, delta=delta, scale=w.scale,
+                  causal=w.causal, stream=stream)
+    elif w.path == "splitkv":
         fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, scale=w.scale, workspace=ws, stream=stream)
     elif w.window_left >= 0:
         fa.fa_fwd_window(q, k, v, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
                          stream=stream)
     else:
         fa.fa_fwd(q, k, v, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+
+
+def make_workspace(fa, w, q, k, v, dev):
+    """Per-path extra buffers, made once outside the timed region."""
+    import torch
+
+    if w.path == "splitkv":
+        return torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
+                           dtype=torch.uint8, device=dev)
+    if w.path == "bwd":
+        from exact_attention_82_gb300.inputs import SEED_BASE, make_qkv
+
+        fo, flse = fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal)
+        dout = make_qkv(w.B, w.H, w.Sq, w.Sk, w.D, SEED_BASE + 999)[0].to(dev)
+        return (fo, flse, dout, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev))
+    return None
 
 
 def run_ours(args, rank, world, local_rank):
@@ -189,10 +211,7 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    ws = None
-    if w.path == "splitkv":
-        ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
-                         dtype=torch.uint8, device=dev)
+    ws = make_workspace(fa, w, dq, dk, dv, dev)
 
     def step():
         run_path(fa, w, dq, dk, dv, o, lse, ws, stream)
@@ -266,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if w.path == "splitkv" else 1),
+        "gpu_launches": args.steps * (2 if w.path in ("splitkv", "bwd") else 1),
         "clocks": clk,
         "impl": "ours",
     }
@@ -280,16 +299,18 @@ def run_e2e(args, w, q, k, v, dev, world):
 
     import exact_attention_82_gb300 as fa
 
+    if w.path == "bwd":
+        return None  # the end-to-end leg times forward outputs; backward runs on device data
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16).pin_memory()
     hl = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
     dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
     do = torch.empty_like(ho, device=dev)
     dl = torch.empty_like(hl, device=dev)
-    ws = None
-    if w.path == "splitkv":
-        ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
-                         dtype=torch.uint8, device=dev)
+    dq.copy_(hq)
+    dk.copy_(hk)
+    dv.copy_(hv)
+    ws = make_workspace(fa, w, dq, dk, dv, dev)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 50))
 

@@ -20,7 +20,8 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_str
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
            "fa_fwd_splitkv", "fa_fwd_splitkv_raw", "fa_fwd_splitkv_workspace_bytes",
-           "fa_splitkv_num_splits", "FA_ERR_SCRATCH_LIMIT"]
+           "fa_splitkv_num_splits", "FA_ERR_SCRATCH_LIMIT",
+           "fa_bwd", "fa_bwd_raw"]
 
 FA_OK = 0
 FA_ERR_NULLPTR = -1
@@ -53,6 +54,7 @@ _SIGNATURES = {
     "fa_fwd_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float,
                                     _i, _vp]),
     "fa_splitkv_num_splits": (_i, [_i, _i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
@@ -211,6 +213,45 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, num_sp
     if st != FA_OK:
         raise FAError(st, "fa_fwd_splitkv")
     return o, lse
+
+
+def fa_bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, do_ptr, dq_ptr, dk_ptr, dv_ptr, delta_ptr,
+               B, H, Sq, Sk, D, scale, causal, stream_ptr) -> int:
+    """The backward C call with raw device pointers; returns the status code."""
+    return lib().fa_bwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, do_ptr, dq_ptr, dk_ptr, dv_ptr,
+                        delta_ptr, B, H, Sq, Sk, D, float(scale), int(causal), stream_ptr)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, delta=None,
+           scale: float | None = None, causal: bool = False, stream=None):
+    """Gradients (dq, dk, dv) of fa_fwd for output gradient ``dout`` (torch CUDA tensors;
+    o and lse are fa_fwd's outputs).  Outputs and the fp32 ``delta`` scratch [B,H,Sq] are
+    allocated if not given.  Returns (dq, dk, dv) without synchronising."""
+    import torch
+
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if delta is None:
+        delta = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    for name, t in (("lse", lse), ("delta", delta)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+    if scale is None:
+        scale = D ** -0.5
+    st = fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                    delta.data_ptr(), B, H, Sq, Sk, D, scale, int(bool(causal)),
+                    _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_device_status(stream=None) -> int:

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["fa_fwd_kernel.cu", "fa_splitkv.cu", "fa_api.cu"]
+SOURCES = ["fa_fwd_kernel.cu", "fa_splitkv.cu", "fa_bwd.cu", "fa_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

@@ -288,12 +288,66 @@ extern "C" int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *
                           stream);
 }
 
+// ------------------------------------------------------------------ backward
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H, int Sq, int Sk,
+                      int D, float scale, int causal, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta) return FA_ERR_NULLPTR;
+    const void *ptrs[10] = {q, k, v, o, lse, dout, dq, dk, dv, delta};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FA_ERR_BAD_SHAPE;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+    if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (!isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+    const long long BH = (long long)B * H;
+    const long long n_qt = (Sq + 127) / 128, n_kt = (Sk + 127) / 128;
+    if (n_qt * BH > 0x7fffffffll || n_kt * BH > 0x7fffffffll) return FA_ERR_BAD_SHAPE;
+    const size_t qb = (size_t)BH * Sq * D * 2, kb = (size_t)BH * Sk * D * 2, lb = (size_t)BH * Sq * 4;
+    // outputs (dq, dk, dv, delta) must not overlap any input or each other
+    const void *outs[4] = {dq, dk, dv, delta};
+    const size_t out_b[4] = {qb, kb, kb, lb};
+    const void *ins[6] = {q, k, v, o, lse, dout};
+    const size_t in_b[6] = {qb, kb, kb, qb, lb, qb};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_b[a], ins[b], in_b[b])) return FA_ERR_ALIAS;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], out_b[a], outs[b], out_b[b])) return FA_ERR_ALIAS;
+    }
+    if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+    if (!encode_bhsd(&tq, q, D, Sq, BH, 128) || !encode_bhsd(&tk, k, D, Sk, BH, 128) ||
+        !encode_bhsd(&tv, v, D, Sk, BH, 128) || !encode_bhsd(&tdo, dout, D, Sq, BH, 128) ||
+        !encode_bhsd(&tdq, dq, D, Sq, BH, 128) || !encode_bhsd(&tdk, dk, D, Sk, BH, 128) ||
+        !encode_bhsd(&tdv, dv, D, Sk, BH, 128))
+        return fail_cuda(cudaErrorInvalidValue);
+    fa::BwdParams p;
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.delta = delta;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.n_qt = (int)n_qt;
+    p.n_kt = (int)n_kt;
+    p.causal = causal;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = kWaitLimitNs;
+    const cudaError_t e = fa::launch_bwd(D, tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return FA_OK;
+}
+
 extern "C" int fa_device_status(void *stream) {
-    int v = 0, w = 0;
+    int v = 0, w = 0, x = 0;
     cudaError_t e = fa::status_read_and_clear(&v, (cudaStream_t)stream);
     if (e == cudaSuccess) e = fa::splitkv_status_read_and_clear(&w);
+    if (e == cudaSuccess) e = fa::bwd_status_read_and_clear(&x);
     if (e != cudaSuccess) return fail_cuda(e);
-    return v != FA_OK ? v : w;
+    return v != FA_OK ? v : (w != FA_OK ? w : x);
 }
 
 extern "C" int fa_selftest_bounded_wait(int timeout_us, void *stream) {

@@ -1,0 +1,539 @@
+// fa_bwd.cu -- attention backward (dQ, dK, dV) for GB300 (sm_103a).
+//
+// For the forward O = softmax(scale Q K^T [+ causal mask]) V with row
+// log-sum-exp LSE, and an output gradient dO:
+//   P = exp(scale Q K^T - LSE)       Delta_i = dO_i . O_i
+//   dV = P^T dO      dP = dO V^T      dS = P (dP - Delta)
+//   dQ = scale dS K  dK = scale dS^T Q
+// "FlashAttention-2 — L3 Cross-Paper Synthesis", §3 items 1-2 (the backward's
+// five products; FA2 accumulates dQ with atomic adds across thread blocks,
+// which makes it non-deterministic) and §5 item 2 (a deterministic two-pass
+// alternative).  Here there are no atomics: two kernels each own their
+// output rows outright.
+//   fa_bwd_dq    one CTA per 128-row query tile, looping over key tiles:
+//                S = Q K^T and dP = dO V^T into tensor memory (TMEM), the
+//                element-wise warps form P and dS, dS goes back over S in
+//                TMEM and feeds dQ += dS K as the MMA's A operand.  It also
+//                writes Delta for the second kernel.
+//   fa_bwd_dkdv  one CTA per 128-key tile, looping over query tiles: S^T =
+//                K Q^T and dP^T = V dO^T; P^T and dS^T go back over them and
+//                feed dV += P^T dO and dK += dS^T Q.
+// P is recomputed from the saved LSE, as the forward's epilogue stores it.
+// Both kernels: warps 0-3 element-wise (thread = TMEM lane = output row),
+// warp 4 TMA producer, warp 5 TMEM allocation and single-thread MMA issue.
+// Rows are handled in 32-column chunks; chunk c's bf16 result is written to
+// columns [16c, 16c+16), all of which the thread has already read.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+__device__ int g_status_bwd = 0;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int T = 128;                      // rows / keys per tile
+    static constexpr int NCH = D / 64;
+    static constexpr uint32_t TILE = T * D * 2;        // one bf16 tile
+    static constexpr uint32_t CHUNK = T * 128;         // 128 rows x 128 bytes
+    // shared memory: two resident tiles, two 2-stage rings, staging reuses the resident tiles
+    static constexpr uint32_t OFF_A = 0;               // resident tile 1 (Q or K)
+    static constexpr uint32_t OFF_B = TILE;            // resident tile 2 (dO or V)
+    static constexpr uint32_t OFF_R1 = 2 * TILE;       // ring 1 (K or Q), 2 stages
+    static constexpr uint32_t OFF_R2 = 4 * TILE;       // ring 2 (V or dO), 2 stages
+    static constexpr uint32_t OFF_VEC = 6 * TILE;      // [2 parity][2: lse2, delta][128] fp32
+    static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * T * 4;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;  // S, dP, accumulator(s)
+    static constexpr uint32_t IDESC_SS = idesc_bf16_f32(T, T, false);  // M=T, N=T, both K-major
+    static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(T, D, true);  // M=T, N=D, B MN-major
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+enum : uint32_t {
+    BB_RES = 0,        // resident tiles loaded
+    BB_FULL = 1,       // + stage (2): ring tiles loaded
+    BB_EMPTY = 3,      // + stage: ring stage free
+    BB_X_FULL = 5,     // S and dP computed
+    BB_P_FULL = 6,     // element-wise results written to TMEM (128 arrivals)
+    BB_DONE = 7,       // last accumulation finished
+    BB_DRAIN = 8,
+};
+constexpr uint32_t BSLOT_TMEM = 128, BSLOT_ABORT = 132;
+constexpr unsigned long long kBwdDrainNs = 20ull * 1000 * 1000;
+
+__device__ __forceinline__ uint32_t b16_pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+// ============================================================ dQ kernel
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (sbase - raw_u32);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mi = (int)(blockIdx.x % (unsigned)p.n_qt);
+    const int bh = (int)(blockIdx.x / (unsigned)p.n_qt);
+    const int mt = p.causal ? (p.n_qt - 1 - mi) : mi;  // causal: longest first
+    const int n_kt = (p.Sk + C::T - 1) / C::T;
+    const int j_hi = p.causal ? min(n_kt - 1, mt) : n_kt - 1;
+    const int N = j_hi + 1;
+    const bool mask_first = p.causal || (p.Sk % C::T) != 0;
+    const uint32_t bars = sbase + C::OFF_BAR;
+    auto bar = [&](uint32_t i) { return bars + 8u * i; };
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_ABORT);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_TMEM);
+    if (threadIdx.x == 0) {
+        mbar_init(bar(BB_RES), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(BB_FULL + s), 1);
+            mbar_init(bar(BB_EMPTY + s), 1);
+        }
+        mbar_init(bar(BB_X_FULL), 1);
+        mbar_init(bar(BB_P_FULL), 128);
+        mbar_init(bar(BB_DONE), 1);
+        mbar_init(bar(BB_DRAIN), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(sbase + C::OFF_BAR + BSLOT_TMEM, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto wait = [&](uint32_t b, uint32_t parity) {
+        return mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT);
+    };
+
+    if (warp == 4) {
+        if (lane == 0) {  // ---- TMA producer: Q, dO once; K_j, V_j per tile (j descending)
+            const uint64_t pol = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(BB_RES), 2 * C::TILE);
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_load_3d(sbase + C::OFF_A + c * C::CHUNK, &tm_q, c * 64, mt * C::T, bh, bar(BB_RES), pol);
+                tma_load_3d(sbase + C::OFF_B + c * C::CHUNK, &tm_do, c * 64, mt * C::T, bh, bar(BB_RES), pol);
+            }
+            int issued = 0;
+            for (int it = 0; it < N; ++it) {
+                const int st = it & 1;
+                if (!wait(BB_EMPTY + st, ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+                mbar_arrive_expect_tx(bar(BB_FULL + st), 2 * C::TILE);
+                const int row = (j_hi - it) * C::T;
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_3d(sbase + C::OFF_R1 + st * C::TILE + c * C::CHUNK, &tm_k, c * 64, row, bh,
+                                bar(BB_FULL + st), pol);
+                    tma_load_3d(sbase + C::OFF_R2 + st * C::TILE + c * C::CHUNK, &tm_v, c * 64, row, bh,
+                                bar(BB_FULL + st), pol);
+                }
+                issued = it + 1;
+            }
+            mbar_wait_drain(bar(BB_RES), 0, kBwdDrainNs);
+            for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
+                mbar_wait_drain(bar(BB_FULL + (it & 1)), (uint32_t)(it >> 1) & 1u, kBwdDrainNs);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {  // ---- MMA issue
+            const uint64_t da = sw128_desc(sbase + C::OFF_A, 16, 1024);   // Q, K-major
+            const uint64_t db = sw128_desc(sbase + C::OFF_B, 16, 1024);   // dO, K-major
+            const uint64_t dk1 = sw128_desc(sbase + C::OFF_R1, 16, 1024);         // K as B of S (K-major)
+            const uint64_t dk2 = sw128_desc(sbase + C::OFF_R1, C::CHUNK, 1024);   // K as B of dQ (MN-major)
+            const uint64_t dv1 = sw128_desc(sbase + C::OFF_R2, 16, 1024);         // V as B of dP (K-major)
+            bool ok = wait(BB_RES, 0);
+            for (int it = 0; ok && it < N; ++it) {
+                const int st = it & 1;
+                ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t so = (st * C::TILE) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(tmem + C::TM_X, da + off, dk1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::TM_Y, db + off, dv1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(BB_X_FULL));
+                ok = wait(BB_P_FULL, (uint32_t)it & 1u);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::T / 16; ++kk)  // A = dS (bf16 in TMEM), B = K (MN-major)
+                    tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + kk * 8, dk2 + so + ((kk * 2048) >> 4),
+                              C::IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(BB_EMPTY + st));
+            }
+            if (ok) tc_commit(bar(BB_DONE));
+            tc_commit(bar(BB_DRAIN));
+            mbar_wait_drain(bar(BB_DRAIN), 0, kBwdDrainNs);
+        }
+    } else {
+        // ---- element-wise warps: thread = query row
+        const int row = threadIdx.x;
+        const int row_g = mt * C::T + row;
+        const bool valid_row = row_g < p.Sq;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t x_tm = tmem + lane_off + C::TM_X, y_tm = tmem + lane_off + C::TM_Y;
+        const uint32_t acc_tm = tmem + lane_off + C::TM_ACC;
+        // Delta_i = dO_i . O_i (also stored for the dK/dV kernel); lse in exp2 units
+        float delta = 0.f, lse2 = INFINITY;
+        if (valid_row) {
+            const size_t r = (size_t)bh * p.Sq + row_g;
+            const uint4 *og = reinterpret_cast<const uint4 *>(p.o) + r * (D / 8);
+            const uint4 *dg = reinterpret_cast<const uint4 *>(p.dout) + r * (D / 8);
+            float acc = 0.f;
+#pragma unroll 4
+            for (int u = 0; u < D / 8; ++u) {
+                const uint4 a = og[u], b = dg[u];
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+                    acc = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(bw[e] & 0xffff0000u), acc);
+                }
+            }
+            delta = acc;
+            p.delta[r] = delta;
+            lse2 = p.lse[r] * 1.4426950408889634f;
+        }
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < N; ++it) {
+            if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int col0 = (j_hi - it) * C::T;
+            const bool masked = it == 0 && mask_first;
+            const int lim = (p.causal ? min(p.Sk, row_g + 1) : p.Sk) - col0;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t s[32], dp[32];
+                tmem_ld32(x_tm + c * 32, s);
+                tmem_ld32(y_tm + c * 32, dp);
+                tmem_ld_wait(s);
+                tmem_ld_wait(dp);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pr[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int cc = c * 32 + 2 * e + h;
+                        float pv = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), sl2, -lse2));
+                        if (!valid_row || (masked && cc >= lim)) pv = 0.f;
+                        pr[h] = pv * (__uint_as_float(dp[2 * e + h]) - delta);
+                    }
+                    pk[c * 16 + e] = b16_pack(pr[0], pr[1]);
+                }
+                tmem_st16(x_tm + c * 16, &pk[c * 16]);
+            }
+            tmem_st_wait64(pk);
+            tc_fence_before();
+            mbar_arrive(bar(BB_P_FULL));
+        }
+        // ---- epilogue: dQ = scale * acc -> bf16 -> shared (the Q tile) -> TMA store
+        if (ok) ok = wait(BB_DONE, 0);
+        ok = __all_sync(0xffffffffu, ok);
+        named_bar_sync(1, 128);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t sO = sbase + C::OFF_A;  // Q is no longer read once every MMA is done
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(acc_tm + c * 32, o);
+                tmem_ld_wait(o);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int U = c * 4 + u;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = b16_pack(__uint_as_float(o[u * 8 + 2 * e]) * p.scale,
+                                        __uint_as_float(o[u * 8 + 2 * e + 1]) * p.scale);
+                    st_shared_v4(sO + (U >> 3) * C::CHUNK + row * 128 + ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4),
+                                 w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (ok && row == 0 && *abort_flag == 0u) {
+            for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_dq, sbase + C::OFF_A + c * C::CHUNK, c * 64, mt * C::T, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ========================================================= dK, dV kernel
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_dkdv(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (sbase - raw_u32);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ni = (int)(blockIdx.x % (unsigned)p.n_kt);
+    const int bh = (int)(blockIdx.x / (unsigned)p.n_kt);
+    const int nt = ni;  // causal: low key tiles see the most query tiles and run first
+    const int i_lo = p.causal ? nt : 0;    // first query tile (causal: the diagonal)
+    const int N = p.n_qt - i_lo;           // query tiles visited
+    const bool mask_first = p.causal;      // only the diagonal tile needs the causal mask
+    const uint32_t bars = sbase + C::OFF_BAR;
+    auto bar = [&](uint32_t i) { return bars + 8u * i; };
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_ABORT);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_TMEM);
+    float *vec = reinterpret_cast<float *>(gbase + C::OFF_VEC);  // [parity][lse2 | delta][128]
+    if (threadIdx.x == 0) {
+        mbar_init(bar(BB_RES), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(BB_FULL + s), 1);
+            mbar_init(bar(BB_EMPTY + s), 1);
+        }
+        mbar_init(bar(BB_X_FULL), 1);
+        mbar_init(bar(BB_P_FULL), 128);
+        mbar_init(bar(BB_DONE), 1);
+        mbar_init(bar(BB_DRAIN), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(sbase + C::OFF_BAR + BSLOT_TMEM, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto wait = [&](uint32_t b, uint32_t parity) {
+        return mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT);
+    };
+    const uint32_t TM_DV = C::TM_ACC, TM_DK = C::TM_ACC + D;
+
+    if (warp == 4) {
+        if (lane == 0) {  // ---- TMA producer: K, V once; Q_i, dO_i per query tile
+            const uint64_t pol = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(BB_RES), 2 * C::TILE);
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_load_3d(sbase + C::OFF_A + c * C::CHUNK, &tm_k, c * 64, nt * C::T, bh, bar(BB_RES), pol);
+                tma_load_3d(sbase + C::OFF_B + c * C::CHUNK, &tm_v, c * 64, nt * C::T, bh, bar(BB_RES), pol);
+            }
+            int issued = 0;
+            for (int it = 0; it < N; ++it) {
+                const int st = it & 1;
+                if (!wait(BB_EMPTY + st, ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+                mbar_arrive_expect_tx(bar(BB_FULL + st), 2 * C::TILE);
+                const int row = (i_lo + it) * C::T;
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_3d(sbase + C::OFF_R1 + st * C::TILE + c * C::CHUNK, &tm_q, c * 64, row, bh,
+                                bar(BB_FULL + st), pol);
+                    tma_load_3d(sbase + C::OFF_R2 + st * C::TILE + c * C::CHUNK, &tm_do, c * 64, row, bh,
+                                bar(BB_FULL + st), pol);
+                }
+                issued = it + 1;
+            }
+            mbar_wait_drain(bar(BB_RES), 0, kBwdDrainNs);
+            for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
+                mbar_wait_drain(bar(BB_FULL + (it & 1)), (uint32_t)(it >> 1) & 1u, kBwdDrainNs);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {  // ---- MMA issue
+            const uint64_t dka = sw128_desc(sbase + C::OFF_A, 16, 1024);          // K, K-major (A of S^T)
+            const uint64_t dva = sw128_desc(sbase + C::OFF_B, 16, 1024);          // V, K-major (A of dP^T)
+            const uint64_t dq1 = sw128_desc(sbase + C::OFF_R1, 16, 1024);         // Q as B of S^T
+            const uint64_t dq2 = sw128_desc(sbase + C::OFF_R1, C::CHUNK, 1024);   // Q as B of dK (MN-major)
+            const uint64_t do1 = sw128_desc(sbase + C::OFF_R2, 16, 1024);         // dO as B of dP^T
+            const uint64_t do2 = sw128_desc(sbase + C::OFF_R2, C::CHUNK, 1024);   // dO as B of dV (MN-major)
+            bool ok = wait(BB_RES, 0);
+            for (int it = 0; ok && it < N; ++it) {
+                const int st = it & 1;
+                ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t so = (st * C::TILE) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(tmem + C::TM_X, dka + off, dq1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::TM_Y, dva + off, do1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(BB_X_FULL));
+                ok = wait(BB_P_FULL, (uint32_t)it & 1u);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::T / 16; ++kk) {
+                    // dV += P^T dO (A = P^T over S^T), dK += dS^T Q (A = dS^T over dP^T)
+                    tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + kk * 8, do2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
+                              (it > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + kk * 8, dq2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
+                              (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(BB_EMPTY + st));
+            }
+            if (ok) tc_commit(bar(BB_DONE));
+            tc_commit(bar(BB_DRAIN));
+            mbar_wait_drain(bar(BB_DRAIN), 0, kBwdDrainNs);
+        }
+    } else {
+        // ---- element-wise warps: thread = key row
+        const int row = threadIdx.x;
+        const int key_g = nt * C::T + row;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t x_tm = tmem + lane_off + C::TM_X, y_tm = tmem + lane_off + C::TM_Y;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < N; ++it) {
+            // this tile's query rows: lse (exp2 units; +inf past Sq, so P = 0) and Delta
+            const int qt = i_lo + it;
+            float *lv = vec + (it & 1) * 256;
+            {
+                const int qg = qt * C::T + row;
+                const size_t r = (size_t)bh * p.Sq + qg;
+                lv[row] = qg < p.Sq ? p.lse[r] * 1.4426950408889634f : INFINITY;
+                lv[128 + row] = qg < p.Sq ? p.delta[r] : 0.f;
+            }
+            named_bar_sync(1, 128);
+            if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                const bool masked = it == 0 && mask_first;  // diagonal: keys above the query are out
+                uint32_t pk[64], dk[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t s[32], dp[32];
+                    tmem_ld32(x_tm + c * 32, s);
+                    tmem_ld32(y_tm + c * 32, dp);
+                    tmem_ld_wait(s);
+                    tmem_ld_wait(dp);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int cc = c * 32 + 2 * e + h;  // query within the tile
+                            float pv = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), sl2, -lv[cc]));
+                            if (masked && key_g > qt * C::T + cc) pv = 0.f;
+                            pr[h] = pv;
+                            ds[h] = pv * (__uint_as_float(dp[2 * e + h]) - lv[128 + cc]);
+                        }
+                        pk[c * 16 + e] = b16_pack(pr[0], pr[1]);
+                        dk[c * 16 + e] = b16_pack(ds[0], ds[1]);
+                    }
+                    tmem_st16(x_tm + c * 16, &pk[c * 16]);
+                    tmem_st16(y_tm + c * 16, &dk[c * 16]);
+                }
+                tmem_st_wait64(pk);
+                tmem_st_wait64(dk);
+                tc_fence_before();
+                mbar_arrive(bar(BB_P_FULL));
+            }
+        }
+        // ---- epilogue: dV and scale * dK -> bf16 -> shared (the K and V tiles) -> TMA store
+        if (ok) ok = wait(BB_DONE, 0);
+        ok = __all_sync(0xffffffffu, ok);
+        named_bar_sync(1, 128);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t src = tmem + lane_off + (which ? TM_DK : TM_DV);
+                const uint32_t sO = sbase + (which ? C::OFF_A : C::OFF_B);
+                const float f = which ? p.scale : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(src + c * 32, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int U = c * 4 + u;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = b16_pack(__uint_as_float(o[u * 8 + 2 * e]) * f, __uint_as_float(o[u * 8 + 2 * e + 1]) * f);
+                        st_shared_v4(sO + (U >> 3) * C::CHUNK + row * 128 + ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4),
+                                     w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (ok && row == 0 && *abort_flag == 0u) {
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_store_3d(&tm_dk, sbase + C::OFF_A + c * C::CHUNK, c * 64, nt * C::T, bh);
+                tma_store_3d(&tm_dv, sbase + C::OFF_B + c * C::CHUNK, c * 64, nt * C::T, bh);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read0();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+int bwd_smem_bytes(int D) { return D == 64 ? (int)BwdCfg<64>::SMEM : (int)BwdCfg<128>::SMEM; }
+
+template <int D>
+static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk,
+                                const CUtensorMap &tdv, const BwdParams &p, long long BH, cudaStream_t stream) {
+    const int smem = (int)BwdCfg<D>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fa_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fa_bwd_dq<D><<<dim3((unsigned)(p.n_qt * BH)), dim3(192), smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    fa_bwd_dkdv<D><<<dim3((unsigned)(p.n_kt * BH)), dim3(192), smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                       const BwdParams &p, long long BH, cudaStream_t stream) {
+    if (D == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, stream);
+    return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, stream);
+}
+
+cudaError_t bwd_status_read_and_clear(int *out) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_bwd, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status_bwd, &zero, sizeof(int));
+    *out = v;
+    return e;
+}
+
+}  // namespace fa

@@ -47,6 +47,24 @@ cudaError_t splitkv_status_read_and_clear(int *out);
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
 cudaError_t splitkv_scratch(void **out);
 
+// Backward launch (dQ kernel, then dK/dV kernel).
+struct BwdParams {
+    const void *o;       // bf16 [B*H, Sq, D]  forward output
+    const void *dout;    // bf16 [B*H, Sq, D]  its gradient
+    const float *lse;    // fp32 [B*H, Sq]     forward log-sum-exp (natural log)
+    float *delta;        // fp32 [B*H, Sq]     workspace: rowsum(dO * O)
+    int Sq, Sk;
+    int n_qt, n_kt;      // 128-row query tiles, 128-key tiles
+    int causal;
+    float scale, scale_log2;
+    unsigned long long timeout_ns;
+};
+int bwd_smem_bytes(int D);
+cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                       const BwdParams &p, long long BH, cudaStream_t stream);
+cudaError_t bwd_status_read_and_clear(int *out);
+
 // Dynamic shared memory the forward kernel for head dim D asks for.
 int fwd_smem_bytes(int D);
 

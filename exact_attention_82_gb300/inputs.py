@@ -34,7 +34,7 @@ class Workload:
     causal: bool
     q_mult: float = 1.0
     window_left: int = -1   # keys i - window_left .. i (+ window_right); -1: unbounded
-    path: str = "fwd"       # "fwd" (query-block parallel) or "splitkv" (decode, key-split)
+    path: str = "fwd"       # "fwd", "splitkv" (decode, key-split) or "bwd" (gradients)
 
     @property
     def window(self):
@@ -55,6 +55,8 @@ class Workload:
             lo = np.maximum(0, i - self.window_left)
             return 4.0 * self.B * self.H * self.D * float(np.maximum(hi - lo + 1, 0).sum())
         f = 4.0 * self.B * self.H * self.Sq * self.Sk * self.D
+        if self.path == "bwd":
+            f *= 2.5  # five products (dV, dP, dQ, dK, and S recomputed) against the forward's two
         return f / 2 if self.causal else f
 
     @property
@@ -69,6 +71,8 @@ class Workload:
             c += f", sliding window of {self.window_left + 1} keys"
         if self.path == "splitkv":
             c += ", split-KV decode"
+        if self.path == "bwd":
+            c += ", backward (dQ, dK, dV)"
         extra = f", Q x{self.q_mult:g}" if self.q_mult != 1.0 else ""
         return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, bf16 N(0,1)"
                 f"{extra}, scale=1/sqrt({self.D}), {c}")
@@ -85,6 +89,9 @@ WORKLOADS = [
     Workload("b2h32s16384d128_swa4096", 2, 32, 16384, 16384, 128, True, 1.0, 4095),
     # decode: one query row per head against a 16384-key cache (HBM-bound)
     Workload("b8h32q1s16384d128_decode", 8, 32, 1, 16384, 128, False, path="splitkv"),
+    # backward of the headline and the causal workloads
+    Workload("b8h16s2048d128_bwd", 8, 16, 2048, 2048, 128, False, path="bwd"),
+    Workload("b4h16s4096d128_causal_bwd", 4, 16, 4096, 4096, 128, True, path="bwd"),
 ]
 
 

@@ -171,6 +171,28 @@ int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
                            int H, int Sq, int Sk, int D, float scale, int num_splits, void *stream);
 
 /*
+ * fa_bwd -- gradients of fa_fwd: given dO = dL/dO for the forward's O,
+ *   P = exp(scale Q K^T - LSE),  Delta_i = dO_i . O_i,  dS = P (dO V^T - Delta),
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ * "FlashAttention-2 — L3 Cross-Paper Synthesis", §3 items 1-2 (the backward
+ * pass; FA2's atomic dQ accumulation is non-deterministic) and §5 item 2 (a
+ * deterministic two-pass backward).  Two kernels run on `stream`: one CTA per
+ * query tile writes dQ and Delta, then one CTA per key tile writes dK and dV.
+ * No atomics: results are bitwise deterministic.
+ *
+ *   q, k, v, B, H, Sq, Sk, D, scale, causal   as passed to fa_fwd
+ *   o, lse        the forward's outputs (bf16 [B,H,Sq,D], fp32 [B,H,Sq])
+ *   dout          bf16 [B,H,Sq,D]
+ *   dq            bf16 [B,H,Sq,D] written;  dk, dv  bf16 [B,H,Sk,D] written
+ *   delta         fp32 [B,H,Sq] caller-owned scratch, written with Delta
+ * All device pointers, 16-byte aligned; outputs may not overlap inputs or one
+ * another.  Errors: those of fa_fwd (full and causal attention only).
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H, int Sq,
+           int Sk, int D, float scale, int causal, void *stream);
+
+/*
  * fa_strerror -- static English text for a status code.  For FA_ERR_CUDA
  * the text of the most recent CUDA error seen by this thread is appended.
  * The returned pointer stays valid until the next call on the same thread.

@@ -156,3 +156,18 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert "16 MiB" in fa.fa_strerror(st)
     assert fa.lib().fa_fwd_splitkv_noalloc(0, *big[1:], 1, 1, 1, 64, 128, 0.1, 0, 0) == \
         fa.FA_ERR_NULLPTR
+
+
+def test_bwd_argument_checks():
+    P = [1 << 20, 1 << 30, 1 << 32, 1 << 34, 1 << 36, 1 << 38, 1 << 40, 1 << 42, 1 << 44, 1 << 46]
+
+    def bcall(ptrs=P, Sq=128, Sk=128, D=64, causal=0, scale=0.125):
+        return fa.fa_bwd_raw(*ptrs, 1, 1, Sq, Sk, D, scale, causal, 0)
+
+    assert bcall(ptrs=[0] + P[1:]) == fa.FA_ERR_NULLPTR
+    assert bcall(ptrs=P[:9] + [P[9] + 4]) == fa.FA_ERR_MISALIGNED
+    assert bcall(D=96) == fa.FA_ERR_UNSUPPORTED_D
+    assert bcall(causal=1, Sq=128, Sk=256) == fa.FA_ERR_UNSUPPORTED_CAUSAL
+    assert bcall(scale=float("nan")) == fa.FA_ERR_BAD_SCALE
+    assert bcall(ptrs=P[:6] + [P[0] + 16] + P[7:]) == fa.FA_ERR_ALIAS   # dq over q
+    assert bcall(ptrs=P[:7] + [P[6]] + P[8:]) == fa.FA_ERR_ALIAS        # dk == dq
