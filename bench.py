@@ -170,6 +170,8 @@ def run_path(fa, w, q, k, v, o, lse, ws, stream):
                   causal=w.causal, stream=stream)
     elif w.path == "splitkv":
         fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, scale=w.scale, workspace=ws, stream=stream)
+    elif w.path == "fp8":
+        fa.fa_fwd_fp8(q, k, v, *ws, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
     elif w.window_left >= 0:
         fa.fa_fwd_window(q, k, v, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
                          stream=stream)
@@ -177,10 +179,25 @@ def run_path(fa, w, q, k, v, o, lse, ws, stream):
         fa.fa_fwd(q, k, v, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
 
 
-def make_workspace(fa, w, q, k, v, dev):
-    """Per-path extra buffers, made once outside the timed region."""
+def workload_inputs(index):
+    """CPU inputs of workload `index`: (q, k, v, descales); descales is None except
+    on the 8-bit path, whose q, k, v are e4m3 codes (uint8)."""
+    from exact_attention_82_gb300.inputs import WORKLOADS, workload_qkv, workload_qkv_fp8
+
+    if WORKLOADS[index].path == "fp8":
+        (q, k, v), ds = workload_qkv_fp8(index)
+        return q, k, v, ds
+    q, k, v = workload_qkv(index)
+    return q, k, v, None
+
+
+def make_workspace(fa, w, q, k, v, dev, descales=None):
+    """Per-path extra buffers (the descales on the 8-bit path), made once outside
+    the timed region."""
     import torch
 
+    if w.path == "fp8":
+        return descales
     if w.path == "splitkv":
         return torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
                            dtype=torch.uint8, device=dev)
@@ -199,19 +216,19 @@ def run_ours(args, rank, world, local_rank):
     import torch.distributed as dist
 
     import exact_attention_82_gb300 as fa
-    from exact_attention_82_gb300.inputs import WORKLOADS, workload_qkv
+    from exact_attention_82_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    q, k, v = workload_qkv(args.workload)
+    q, k, v, descales = workload_inputs(args.workload)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    ws = make_workspace(fa, w, dq, dk, dv, dev)
+    ws = make_workspace(fa, w, dq, dk, dv, dev, descales)
 
     def step():
         run_path(fa, w, dq, dk, dv, o, lse, ws, stream)
@@ -247,10 +264,10 @@ def run_ours(args, rank, world, local_rank):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status after timing: {fa.fa_strerror(st)}")
 
-    e2e = None if args.no_e2e else run_e2e(args, w, q, k, v, dev, world)
+    e2e = None if args.no_e2e else run_e2e(args, w, q, k, v, dev, world, descales)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, q, k, v, args.cpu_seconds)
+        cpu = cpu_baseline(w, q, k, v, args.cpu_seconds, descales)
     if rank != 0:
         return None
     peaks, which = measured_peaks()
@@ -266,6 +283,15 @@ def run_ours(args, rank, world, local_rank):
                     "frac": round(gbs / hbm_peak, 4),
                     "peak_source": f"{which}: hbm_gbs (copy bandwidth)" if peaks
                     else "fallback: 6.8 TB/s", "traffic": traffic}
+    elif w.path == "fp8":
+        # e4m3 contractions: the measured bf16 peak times the nominal 8-bit : 16-bit
+        # dense ratio (4.5 : 2.25 PFLOP/s)
+        peak8 = 2.0 * peak
+        roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2), "peak": peak8,
+                    "unit": "TFLOP/s", "frac": round(tflops_launch / peak8, 4),
+                    "peak_source": (f"{which}: bf16_tflops (burst, cuBLAS bf16 GEMM)" if peaks
+                                    else "fallback: 1.9 PFLOP/s bf16")
+                    + " x 2, the nominal fp8/bf16 dense ratio", "traffic": traffic}
     else:
         roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(tflops_launch / peak, 4),
@@ -274,8 +300,8 @@ def run_ours(args, rank, world, local_rank):
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.path == "fp8" else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "desc": w.describe(), "B": w.B, "H": w.H, "Sq": w.Sq,
                    "Sk": w.Sk, "D": w.D, "causal": w.causal, "window": list(w.window),
                    "parallelism": f"independent workload per GPU x{world}",
@@ -291,7 +317,7 @@ def run_ours(args, rank, world, local_rank):
     }
 
 
-def run_e2e(args, w, q, k, v, dev, world):
+def run_e2e(args, w, q, k, v, dev, world, descales=None):
     """Same metric through the public call with host buffers: every step copies
     Q, K, V from pinned host memory, runs fa_fwd and reads O and LSE back."""
     import torch
@@ -310,7 +336,7 @@ def run_e2e(args, w, q, k, v, dev, world):
     dq.copy_(hq)
     dk.copy_(hk)
     dv.copy_(hv)
-    ws = make_workspace(fa, w, dq, dk, dv, dev)
+    ws = make_workspace(fa, w, dq, dk, dv, dev, descales)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 50))
 
@@ -350,8 +376,9 @@ def _host_cores():
         return os.cpu_count() or 1
 
 
-def _oracle_sample(w, qb, kb, vb, heads):
-    """Oracle over the first `heads` (b,h) pairs, all rows; returns (seconds, flops)."""
+def _oracle_sample(w, qb, kb, vb, heads, descales=None):
+    """Oracle over the first `heads` (b,h) pairs, all rows; returns (seconds, flops).
+    qb, kb, vb: bf16 bit patterns, or e4m3 codes when `descales` is given."""
     import oracle
 
     BH = w.B * w.H
@@ -359,24 +386,32 @@ def _oracle_sample(w, qb, kb, vb, heads):
     ks = kb.reshape(BH, w.Sk, w.D)[:heads][None]
     vs = vb.reshape(BH, w.Sk, w.D)[:heads][None]
     t0 = time.perf_counter()
-    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, w.window, nthreads=_host_cores())
+    if descales is not None:
+        oracle.attn_fwd_fp8(qs, ks, vs, *descales, w.scale, w.causal, nthreads=_host_cores())
+    else:
+        oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, w.window, nthreads=_host_cores())
     dt = time.perf_counter() - t0
     return dt, w.flops / BH * heads
 
 
-def cpu_baseline(w, q, k, v, target_s):
+def _oracle_inputs(q, k, v, descales):
+    from exact_attention_82_gb300.inputs import bf16_bits, u8_codes
+
+    conv = u8_codes if descales is not None else bf16_bits
+    return conv(q), conv(k), conv(v)
+
+
+def cpu_baseline(w, q, k, v, target_s, descales=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the
     same workload: whole heads, grown until about `target_s` seconds."""
-    from exact_attention_82_gb300.inputs import bf16_bits
-
-    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    qb, kb, vb = _oracle_inputs(q, k, v, descales)
     cores = _host_cores()
     BH = w.B * w.H
     heads = min(BH, cores)
-    dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+    dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
     if dt < target_s / 4 and heads < BH:
         heads = min(BH, max(heads + 1, int(heads * target_s / max(dt, 1e-3) * 0.8)))
-        dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+        dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": f"{heads} of {BH} (batch,head) pairs of {w.name}, every query row; "
@@ -386,21 +421,21 @@ def cpu_baseline(w, q, k, v, target_s):
 def run_reference(args):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
     sample (whole heads) of the same workload."""
-    from exact_attention_82_gb300.inputs import WORKLOADS, bf16_bits, workload_qkv
+    from exact_attention_82_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
-    q, k, v = workload_qkv(args.workload)
-    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    q, k, v, descales = workload_inputs(args.workload)
+    qb, kb, vb = _oracle_inputs(q, k, v, descales)
     cores = _host_cores()
     heads = min(w.B * w.H, cores)
     # size a step to about 3 s of host work, from the first warm-up step
-    dt, _ = _oracle_sample(w, qb, kb, vb, heads)
+    dt, _ = _oracle_sample(w, qb, kb, vb, heads, descales)
     heads = max(1, min(w.B * w.H, int(heads * 3.0 / max(dt, 1e-3))))
     for _ in range(args.warmup - 1):
-        _oracle_sample(w, qb, kb, vb, heads)
+        _oracle_sample(w, qb, kb, vb, heads, descales)
     tot_t, tot_f = 0.0, 0.0
     for _ in range(args.steps):
-        dt, fl = _oracle_sample(w, qb, kb, vb, heads)
+        dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
         tot_t += dt
         tot_f += fl
     value = tot_f / tot_t / 1e12

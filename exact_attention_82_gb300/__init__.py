@@ -21,7 +21,7 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_str
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
            "fa_fwd_splitkv", "fa_fwd_splitkv_raw", "fa_fwd_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "FA_ERR_SCRATCH_LIMIT",
-           "fa_bwd", "fa_bwd_raw"]
+           "fa_bwd", "fa_bwd_raw", "fa_fwd_fp8", "fa_fwd_fp8_raw"]
 
 FA_OK = 0
 FA_ERR_NULLPTR = -1
@@ -55,6 +55,8 @@ _SIGNATURES = {
                                     _i, _vp]),
     "fa_splitkv_num_splits": (_i, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i,
+                        ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
@@ -212,6 +214,50 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, num_sp
                             _stream_ptr(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_splitkv")
+    return o, lse
+
+
+def fa_fwd_fp8_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+                   Sq: int, Sk: int, D: int, scale: float, causal: int, descale_q: float,
+                   descale_k: float, descale_v: float, stream_ptr: int) -> int:
+    """The 8-bit C call with raw device pointers; returns the status code."""
+    return lib().fa_fwd_fp8(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
+                            int(causal), float(descale_q), float(descale_k), float(descale_v),
+                            stream_ptr)
+
+
+def fa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, o=None, lse=None,
+               scale: float | None = None, causal: bool = False, stream=None):
+    """Attention forward on e4m3 inputs with per-tensor scales (real value = code * descale).
+
+    q: [B,H,Sq,128], k, v: [B,H,Sk,128], each a contiguous CUDA tensor of dtype uint8
+    (the codes) or torch.float8_e4m3fn.  o (bf16 [B,H,Sq,128]) and lse (fp32 [B,H,Sq])
+    are allocated if not given.  Returns (o, lse) without synchronising."""
+    import torch
+
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_cuda or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA uint8 / float8_e4m3fn tensor")
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] matching q")
+    if o is None:
+        o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if o.dtype != torch.bfloat16 or tuple(o.shape) != (B, H, Sq, D) or not o.is_contiguous() \
+            or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq) or \
+            not lse.is_contiguous() or not o.is_cuda or not lse.is_cuda:
+        raise ValueError("o must be contiguous CUDA bf16 [B,H,Sq,D] and lse fp32 [B,H,Sq]")
+    if scale is None:
+        scale = D ** -0.5
+    st = fa_fwd_fp8_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, Sq, Sk, D, scale, int(bool(causal)), descale_q, descale_k,
+                        descale_v, _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return o, lse
 
 

@@ -47,17 +47,19 @@ bool get_encoder() {
     return g_encode != nullptr;
 }
 
-// 3-D map over a [BH, S, D] bf16 tensor: dims (D, S, BH), box (64, rows, 1),
-// 128-byte swizzle, zero fill outside the tensor.  Being 3-D, a box never
-// reaches into the next head's rows.
-bool encode_bhsd(CUtensorMap *map, const void *ptr, int D, int S, long long BH, int box_rows) {
+// 3-D map over a [BH, S, D] tensor of bf16 (eb = 2) or 8-bit (eb = 1)
+// elements: dims (D, S, BH), box (128 bytes of a row, rows, 1), 128-byte
+// swizzle, zero fill outside the tensor.  Being 3-D, a box never reaches into
+// the next head's rows.
+bool encode_bhsd(CUtensorMap *map, const void *ptr, int D, int S, long long BH, int box_rows, int eb = 2) {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2u, (cuuint64_t)S * (cuuint64_t)D * 2u};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)S * (cuuint64_t)D * eb};
+    const cuuint32_t box[3] = {128u / (cuuint32_t)eb, (cuuint32_t)box_rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = g_encode(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                                const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -78,10 +80,10 @@ extern "C" const char *fa_strerror(int status) {
         case FA_OK: s = "ok"; break;
         case FA_ERR_NULLPTR: s = "a required pointer is NULL"; break;
         case FA_ERR_BAD_SHAPE: s = "bad shape: B, H, Sq, Sk must be >= 1 and sizes in range"; break;
-        case FA_ERR_UNSUPPORTED_D: s = "unsupported head dim (64 or 128)"; break;
+        case FA_ERR_UNSUPPORTED_D: s = "unsupported head dim (64 or 128; 128 for the 8-bit path)"; break;
         case FA_ERR_UNSUPPORTED_CAUSAL: s = "causal must be 0 or 1, and causal needs Sq == Sk"; break;
         case FA_ERR_MISALIGNED: s = "a pointer is not 16-byte aligned"; break;
-        case FA_ERR_BAD_SCALE: s = "scale must be finite and > 0"; break;
+        case FA_ERR_BAD_SCALE: s = "scale (and each descale) must be finite and > 0"; break;
         case FA_ERR_CUDA: s = "CUDA error"; break;
         case FA_ERR_TIMEOUT: s = "an on-chip wait gave up (bounded-wait timeout)"; break;
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
@@ -143,6 +145,7 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.wl = wl < 0 ? -1 : wl;
     p.wr = wr < 0 ? -1 : wr;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.o_scale = 1.f;
     p.timeout_ns = kWaitLimitNs;
     const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, n_mblk * BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
@@ -166,6 +169,52 @@ extern "C" int fa_fwd_window(const void *q, const void *k, const void *v, void *
     if (window_left < -1 || window_right < -1) return FA_ERR_BAD_WINDOW;
     if ((window_left >= 0 || window_right >= 0) && Sq != Sk) return FA_ERR_BAD_WINDOW;
     return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream);
+}
+
+extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                          int Sq, int Sk, int D, float scale, int causal, float descale_q, float descale_k,
+                          float descale_v, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_NULLPTR;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FA_ERR_BAD_SHAPE;
+    if (D != 128) return FA_ERR_UNSUPPORTED_D;
+    if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
+    const float sc[4] = {scale, descale_q, descale_k, descale_v};
+    for (float x : sc)
+        if (!isfinite(x) || !(x > 0.f)) return FA_ERR_BAD_SCALE;
+    const float scale_log2 = scale * descale_q * descale_k * 1.4426950408889634f;
+    if (!isfinite(scale_log2) || !(scale_log2 > 0.f)) return FA_ERR_BAD_SCALE;
+    const long long BH = (long long)B * H;
+    const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
+    if (BH > (1ll << 31) || n_mblk * BH > 0x7fffffffll) return FA_ERR_BAD_SHAPE;
+    const size_t q_bytes = (size_t)BH * Sq * D, kv_bytes = (size_t)BH * Sk * D;
+    const size_t o_bytes = 2 * q_bytes, lse_bytes = (size_t)BH * Sq * 4;
+    if (overlaps(o, o_bytes, q, q_bytes) || overlaps(o, o_bytes, k, kv_bytes) || overlaps(o, o_bytes, v, kv_bytes) ||
+        overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+        overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, o, o_bytes))
+        return FA_ERR_ALIAS;
+    if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    if (!encode_bhsd(&tm_q, q, D, Sq, BH, fa::kBlockM, 1) || !encode_bhsd(&tm_k, k, D, Sk, BH, fa::kBlockN, 1) ||
+        !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN, 1) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
+        return fail_cuda(cudaErrorInvalidValue);
+    fa::FwdParams p;
+    p.lse = lse;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.n_mblk = (int)n_mblk;
+    p.n_kv = (Sk + fa::kBlockN - 1) / fa::kBlockN;
+    p.causal = causal;
+    p.wl = -1;
+    p.wr = causal ? 0 : -1;
+    p.scale_log2 = scale_log2;
+    p.o_scale = descale_v;
+    p.timeout_ns = kWaitLimitNs;
+    const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, tm_o, p, n_mblk * BH, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return FA_OK;
 }
 
 // ------------------------------------------------------------- split-KV path

@@ -55,32 +55,51 @@ namespace fa {
 
 __device__ int g_status_word = 0;
 
-template <int D>
+template <int D, bool F8>
 struct FwdCfg {
     static constexpr int BM = kBlockM;  // rows per sub-tile (TMEM lanes)
     static constexpr int BN = kBlockN;  // keys per K/V tile
-    static constexpr int KST = (D == 128) ? 3 : 4;
-    static constexpr int VST = (D == 128) ? 2 : 4;
-    static constexpr int NCH = D / 64;                    // 128-byte column chunks per row
-    static constexpr uint32_t QT_BYTES = BM * D * 2;      // one query sub-tile
-    static constexpr uint32_t KV_BYTES = BN * D * 2;      // one K or V tile
+    static constexpr int EB = F8 ? 1 : 2;                 // bytes per Q/K/V element
+    static constexpr int KST = (F8 || D == 64) ? 4 : 3;
+    static constexpr int VST = (F8 || D == 64) ? 4 : 2;
+    static constexpr int NCH = D * EB / 128;              // 128-byte column chunks per Q/K/V row
+    static constexpr int CH_ELEMS = 128 / EB;             // elements per chunk
+    static constexpr int O_NCH = D / 64;                  // 128-byte chunks per bf16 O row
+    static constexpr uint32_t QT_BYTES = BM * D * EB;     // one query sub-tile
+    static constexpr uint32_t KV_BYTES = BN * D * EB;     // one K or V tile
+    static constexpr uint32_t OT_BYTES = BM * D * 2;      // one bf16 output sub-tile
     static constexpr uint32_t CHUNK = 128 * 128;          // 128 rows x 128 bytes
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
+    // bf16 stages O in its own (then free) Q buffer; an 8-bit one is too small
+    static constexpr uint32_t OFF_O = F8 ? OFF_V + VST * KV_BYTES : OFF_Q;
+    static constexpr uint32_t OFF_BAR = F8 ? OFF_O + 2 * OT_BYTES : OFF_V + VST * KV_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256;
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
-    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, true);
+    // one MMA takes 32 bytes of the contraction: 16 bf16 or 32 e4m3 elements
+    static constexpr int S_STEPS = D * EB / 32;
+    static constexpr int PV_STEPS = BN * EB / 32;
+    static constexpr uint32_t V_STEP = (32 / EB) * 128;   // V bytes per PV step (keys x 128 B)
+    static constexpr uint32_t IDESC_S = F8 ? idesc_e4m3_f32(BM, BN, false) : idesc_bf16_f32(BM, BN, false);
+    static constexpr uint32_t IDESC_PV = F8 ? idesc_e4m3_f32(BM, D, true) : idesc_bf16_f32(BM, D, true);
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!F8 || D == 128, "8-bit rows must fill one 128-byte swizzle atom");
     static_assert(BM == 128 && BN == 128, "tile");
-    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_O % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(SMEM > 114 * 1024, "one CTA per SM (it takes all TMEM columns)");
 };
+
+// 8-bit path: P is stored as e4m3 scaled by 2^kF8PShift, and the running max
+// only moves when a tile's max exceeds it by more than kF8Lazy (exp2 units),
+// so every stored value is at most 2^(kF8Lazy + kF8PShift) = 256 <= 448, the
+// largest finite e4m3, while values down to 2^-16 of the running max stay
+// representable (e4m3's smallest subnormal is 2^-9).
+constexpr float kF8PShift = 6.f;
+constexpr float kF8Lazy = 2.f;
 
 // barrier slots (8 bytes each) inside the OFF_BAR block
 enum : uint32_t {
@@ -107,12 +126,14 @@ static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register spli
 // WIN: a bounded key band (window_left >= 0 or window_right > 0).  Without it
 // (full or causal attention) only a sub-tile's first key tile can need a mask
 // and every row has an allowed key in it, which the code below exploits.
-template <int D, bool WIN>
+// F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
+template <int D, bool WIN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, F8>;
+    static_assert(!(F8 && WIN), "the 8-bit path has no bounded band");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -197,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < 2; ++t)
                 if (act[t])
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * 64, row0 + t * C::BM, bh,
+                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS, row0 + t * C::BM, bh,
                                     bar(B_Q_FULL), pol_q);
             int nk = 0, nv = 0;  // loads issued
             auto load_k = [&](int it) -> bool {
@@ -205,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(B_K_EMPTY + st, ((uint32_t)(it / C::KST) & 1u) ^ 1u)) return false;
                 mbar_arrive_expect_tx(bar(B_K_FULL + st), C::KV_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tm_k, c * 64, (J - it) * C::BN, bh,
+                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tm_k, c * C::CH_ELEMS, (J - it) * C::BN, bh,
                                 bar(B_K_FULL + st), pol_kv);
                 nk = it + 1;
                 return true;
@@ -215,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(B_V_EMPTY + st, ((uint32_t)(it / C::VST) & 1u) ^ 1u)) return false;
                 mbar_arrive_expect_tx(bar(B_V_FULL + st), C::KV_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tm_v, c * 64, (J - it) * C::BN, bh,
+                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tm_v, c * C::CH_ELEMS, (J - it) * C::BN, bh,
                                 bar(B_V_FULL + st), pol_kv);
                 nv = it + 1;
                 return true;
@@ -253,9 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t kph = 0, vph = 0, vpph = 0;
             auto issue_s = [&](uint64_t dq, uint32_t s_tm) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < C::S_STEPS; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-                    tc_mma_ss(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+                    if constexpr (F8)
+                        tc_mma_ss_f8(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+                    else
+                        tc_mma_ss(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int npv, int stage, uint32_t phase) -> bool {
@@ -264,10 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    // A = P_t in TMEM (8 columns = 16 keys per step); B = V, MN-major
-                    tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * 2048) >> 4),
-                              C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                    // A = P_t in TMEM (8 columns = 32 bytes of keys per step); B = V, MN-major
+                    if constexpr (F8)
+                        tc_mma_ts_f8(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
+                                     C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
+                    else
+                        tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
+                                  C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
+                }
                 return true;
             };
             for (int it = 0; ok && it < N; ++it) {
@@ -360,16 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c * 32 + e < lim_lo || c * 32 + e >= lim_hi) s[c][e] = __float_as_uint(-INFINITY);
                 };
                 if (masked) apply_mask();
-                // P is computed against the max already in use.  The row max is
-                // only taken on the first tile, or again for a tile whose sum shows
-                // a score more than 2^64 above that max (the sum also catches inf
-                // and NaN): then the tile is redone against its true max.  S is
-                // still intact in TMEM then, because P is stored after the check.
-                const uint64_t c2 = f2_pack(sl2, sl2);
-                float alpha = 1.f, sum = 0.f;
-                uint32_t pk[64];
-                auto take_max = [&]() {
-                    // row max: four independent chains of three-input max
+                if constexpr (F8) {
+                    // The tile's row max every tile; the running max moves only when
+                    // it is exceeded by more than kF8Lazy, and O is then rescaled.
                     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -379,65 +401,136 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int q = 0; q < 4; ++q)
                                 mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
                                               __uint_as_float(s[c][e + 2 * q + 1]));
-                    const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
-                    // 0 on a row's first keys; 1 while a row has seen no allowed key
-                    alpha = (WIN && m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
-                    m_used = m_new;
-                };
-                auto exp_pass = [&]() {
-                    // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
-                    // row sum in four packed partial sums
-                    const float nm = (WIN && m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
+                    const float m_tile = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2;
+                    const bool move = m_tile > m_used + kF8Lazy;  // always on the first tile
+                    float alpha = 1.f;
+                    if (move) {
+                        alpha = ex2_approx(m_used - m_tile);  // 0 on the first tile
+                        m_used = m_tile;
+                    }
+                    // p' = 2^(s*scale*log2e - m + kF8PShift) <= 256, packed four
+                    // keys to a TMEM column (lowest key in the lowest byte)
+                    const uint64_t c2 = f2_pack(sl2, sl2);
+                    const float nm = kF8PShift - m_used;
                     const uint64_t nm2 = f2_pack(nm, nm);
                     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                    uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float x0, x1;
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
+                        for (int e = 0; e < 8; ++e) {
+                            float x0, x1, x2, x3;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][4 * e]), __uint_as_float(s[c][4 * e + 1])),
                                              c2, nm2),
                                       x0, x1);
-                            const float p0 = ex2_approx(x0);
-                            const float p1 = ex2_approx(x1);
-                            acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-                            pk[c * 16 + e] = pack_bf16x2(p0, p1);
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][4 * e + 2]),
+                                                     __uint_as_float(s[c][4 * e + 3])),
+                                             c2, nm2),
+                                      x2, x3);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                            acc[(2 * e) & 3] = f2_add(acc[(2 * e) & 3], f2_pack(p0, p1));
+                            acc[(2 * e + 1) & 3] = f2_add(acc[(2 * e + 1) & 3], f2_pack(p2, p3));
+                            pk[c * 8 + e] = pack_e4m3x4(p0, p1, p2, p3);
                         }
                     float a0, a1, b0, b1;
                     f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
                     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-                    sum = (a0 + a1) + (b0 + b1);
-                };
-                // the max is taken while any row of the warp has no allowed key
-                // yet (always on the first tile)
-                const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
-                if (took_max) take_max();
-                exp_pass();
-                const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
-                if (redo) {
+                    tmem_st32(s_tm, pk);
+                    tmem_st_wait(pk);
+                    l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
+                    if (i > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(o_tm + c * 32, o);
+                            tmem_ld_wait(o);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-                    if (masked) apply_mask();
-                    take_max();
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(o_tm + c * 32, o);
+                            tmem_st_wait(o);
+                        }
+                    }
+                } else {
+                    // P is computed against the max already in use.  The row max is
+                    // only taken on the first tile, or again for a tile whose sum shows
+                    // a score more than 2^64 above that max (the sum also catches inf
+                    // and NaN): then the tile is redone against its true max.  S is
+                    // still intact in TMEM then, because P is stored after the check.
+                    const uint64_t c2 = f2_pack(sl2, sl2);
+                    float alpha = 1.f, sum = 0.f;
+                    uint32_t pk[64];
+                    auto take_max = [&]() {
+                        // row max: four independent chains of three-input max
+                        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c)
+    #pragma unroll
+                            for (int e = 0; e < 32; e += 8)
+    #pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
+                                                  __uint_as_float(s[c][e + 2 * q + 1]));
+                        const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
+                        // 0 on a row's first keys; 1 while a row has seen no allowed key
+                        alpha = (WIN && m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+                        m_used = m_new;
+                    };
+                    auto exp_pass = [&]() {
+                        // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
+                        // row sum in four packed partial sums
+                        const float nm = (WIN && m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
+                        const uint64_t nm2 = f2_pack(nm, nm);
+                        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c)
+    #pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                float x0, x1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
+                                                 c2, nm2),
+                                          x0, x1);
+                                const float p0 = ex2_approx(x0);
+                                const float p1 = ex2_approx(x1);
+                                acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+                                pk[c * 16 + e] = pack_bf16x2(p0, p1);
+                            }
+                        float a0, a1, b0, b1;
+                        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+                        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+                        sum = (a0 + a1) + (b0 + b1);
+                    };
+                    // the max is taken while any row of the warp has no allowed key
+                    // yet (always on the first tile)
+                    const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
+                    if (took_max) take_max();
                     exp_pass();
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
-                tmem_st_wait64(pk);
-                l_run = l_run * alpha + sum;
-                if (redo || (WIN && took_max && i > 0)) {
-                    // O holds the earlier tiles relative to the old max: rescale it
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(o_tm + c * 32, o);
-                        tmem_ld_wait(o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(o_tm + c * 32, o);
-                        tmem_st_wait(o);
+                    const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
+                    if (redo) {
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                        if (masked) apply_mask();
+                        take_max();
+                        exp_pass();
+                    }
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
+                    tmem_st_wait64(pk);
+                    l_run = l_run * alpha + sum;
+                    if (redo || (WIN && took_max && i > 0)) {
+                        // O holds the earlier tiles relative to the old max: rescale it
+    #pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(o_tm + c * 32, o);
+                            tmem_ld_wait(o);
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(o_tm + c * 32, o);
+                            tmem_st_wait(o);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -452,10 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // buffer, free once its last MMA is done) -> TMA store; LSE.  Both
         // named barriers run whatever `ok` says, so no warp can be left waiting.
         named_bar_sync(1 + t, 128);
-        const uint32_t sO = sQ + t * C::QT_BYTES;
+        const uint32_t sO = sbase + C::OFF_O + t * C::OT_BYTES;
         if (my_act && ok) {
             tc_fence_after();
-            const float inv_l = 1.f / l_run;
+            // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
+            const float inv_l = (F8 ? p.o_scale : 1.f) / l_run;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -479,13 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1 + t, 128);
         if (my_act && ok && row == 0 && *abort_flag == 0u) {
 #pragma unroll
-            for (int c = 0; c < C::NCH; ++c)
+            for (int c = 0; c < C::O_NCH; ++c)
                 tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, row0 + t * C::BM, bh);
             bulk_commit_group();
             bulk_wait_group_read0();
         }
         if (my_act && ok && row_g < p.Sq)
-            p.lse[(size_t)bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
+            p.lse[(size_t)bh * p.Sq + row_g] =
+                (m_used - (F8 ? kF8PShift : 0.f) + lg2_approx(l_run)) * 0.69314718055994531f;
     }
 
     tc_fence_before();
@@ -515,18 +610,18 @@ __global__ void fa_wait_selftest(unsigned long long limit_ns) {
 }
 
 int fwd_smem_bytes(int D) {
-    return D == 64 ? (int)FwdCfg<64>::SMEM : (int)FwdCfg<128>::SMEM;
+    return D == 64 ? (int)FwdCfg<64, false>::SMEM : (int)FwdCfg<128, false>::SMEM;
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool F8>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas,
                                 cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)FwdCfg<D>::SMEM);
+    constexpr uint32_t smem = FwdCfg<D, F8>::SMEM;
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fa_fwd_sm103a<D, WIN><<<dim3((unsigned)n_ctas), dim3(kThreads), FwdCfg<D>::SMEM, stream>>>(tm_q, tm_k,
-                                                                                             tm_v, tm_o, p);
+    fa_fwd_sm103a<D, WIN, F8><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, tm_o, p);
     return cudaGetLastError();
 }
 
@@ -534,10 +629,15 @@ cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, 
                        const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
     if (D == 64)
-        return win ? launch_fwd_d<64, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-                   : launch_fwd_d<64, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    return win ? launch_fwd_d<128, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-               : launch_fwd_d<128, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+        return win ? launch_fwd_d<64, true, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+                   : launch_fwd_d<64, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    return win ? launch_fwd_d<128, true, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+               : launch_fwd_d<128, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream) {
+    return launch_fwd_d<128, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
 }
 
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream) {

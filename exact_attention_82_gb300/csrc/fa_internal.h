@@ -19,7 +19,8 @@ struct FwdParams {
     int n_kv;          // ceil(Sk / kBlockN)
     int causal;        // longest-first query-block order (triangular work)
     int wl, wr;        // key j allowed for query i iff i-wl <= j <= i+wr; -1 = unbounded
-    float scale_log2;  // scale * log2(e)
+    float scale_log2;  // scale * log2(e)  (8-bit path: times descale_q * descale_k)
+    float o_scale;     // 8-bit path: descale_v (unused by the bf16 path)
     unsigned long long timeout_ns;  // bound of every on-chip wait
 };
 
@@ -72,6 +73,10 @@ int fwd_smem_bytes(int D);
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                        const CUtensorMap &tm_v, const CUtensorMap &tm_o, const FwdParams &p,
                        long long n_ctas, cudaStream_t stream);
+
+// Launch the 8-bit (e4m3 Q, K, V; D = 128; full or causal) forward kernel.
+cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream);
 
 // Device status word: read it (after synchronising `stream`) and reset it.
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream);

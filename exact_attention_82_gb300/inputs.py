@@ -2,14 +2,18 @@
 
 This module is shared by the CUDA path (tests, bench, smoke check) and by the
 oracle's tests.  It holds none of the attention arithmetic: only the workload
-table, seeded normal draws and the rounding of those draws to bf16.
+table, seeded normal draws and the rounding of those draws to bf16 or e4m3.
 
-Recipe (the pages fix none of it; all five workloads are i.i.d. N(0, 1)):
+Recipe (the pages fix none of it; every workload draws i.i.d. N(0, 1)):
   * a torch CPU ``Generator`` seeded with ``seed``;
   * Q, then K, then V, each drawn as float32 ``randn`` of its full shape and
     rounded to bf16 (round-to-nearest-even, torch's ``.to(bfloat16)``);
   * for the peaky-softmax workload Q is then multiplied by 4, which is exact
     in bf16 (a power of two, far from overflow).
+  * 8-bit (e4m3) inputs: the same float32 draws, each tensor given its own
+    scale (descale = amax / 448, 448 being e4m3's largest finite value) and
+    rounded to e4m3 codes by torch's ``.to(float8_e4m3fn)``; the codes travel
+    as uint8 and the real value is code * descale.
 Workload i uses seed ``SEED_BASE + i``.
 """
 from __future__ import annotations
@@ -34,7 +38,7 @@ class Workload:
     causal: bool
     q_mult: float = 1.0
     window_left: int = -1   # keys i - window_left .. i (+ window_right); -1: unbounded
-    path: str = "fwd"       # "fwd", "splitkv" (decode, key-split) or "bwd" (gradients)
+    path: str = "fwd"       # "fwd", "splitkv" (decode, key-split), "bwd" (gradients), "fp8"
 
     @property
     def window(self):
@@ -62,7 +66,8 @@ class Workload:
     @property
     def hbm_bytes(self) -> float:
         """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
-        return float(self.B * self.H * (2 * (self.Sq + 2 * self.Sk) * self.D + 2 * self.Sq * self.D
+        eb = 1 if self.path == "fp8" else 2
+        return float(self.B * self.H * (eb * (self.Sq + 2 * self.Sk) * self.D + 2 * self.Sq * self.D
                                         + 4 * self.Sq))
 
     def describe(self) -> str:
@@ -74,7 +79,8 @@ class Workload:
         if self.path == "bwd":
             c += ", backward (dQ, dK, dV)"
         extra = f", Q x{self.q_mult:g}" if self.q_mult != 1.0 else ""
-        return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, bf16 N(0,1)"
+        dt = "e4m3 (per-tensor scale)" if self.path == "fp8" else "bf16"
+        return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, {dt} N(0,1)"
                 f"{extra}, scale=1/sqrt({self.D}), {c}")
 
 
@@ -92,6 +98,9 @@ WORKLOADS = [
     # backward of the headline and the causal workloads
     Workload("b8h16s2048d128_bwd", 8, 16, 2048, 2048, 128, False, path="bwd"),
     Workload("b4h16s4096d128_causal_bwd", 4, 16, 4096, 4096, 128, True, path="bwd"),
+    # 8-bit (e4m3) Q, K, V with per-tensor scales, the headline shape and causal
+    Workload("b8h16s2048d128_fp8", 8, 16, 2048, 2048, 128, False, path="fp8"),
+    Workload("b4h16s4096d128_causal_fp8", 4, 16, 4096, 4096, 128, True, path="fp8"),
 ]
 
 
@@ -107,10 +116,46 @@ def make_qkv(B: int, H: int, Sq: int, Sk: int, D: int, seed: int, q_mult: float 
     return q, k, v
 
 
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor scaling of a float32 CPU tensor to e4m3: returns (uint8 codes,
+    descale) with descale = amax / 448 as a float32 value (1.0 for an all-zero
+    tensor) and codes = round-to-nearest(x / descale) in e4m3."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    descale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+    y = (x.to(torch.float32) / descale).clamp(-E4M3_MAX, E4M3_MAX)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), descale
+
+
+def make_qkv_fp8(B: int, H: int, Sq: int, Sk: int, D: int, seed: int, q_mult: float = 1.0):
+    """e4m3 codes (uint8 CPU tensors) q [B,H,Sq,D], k and v [B,H,Sk,D] and their
+    descales (dq, dk, dv), from the same draws as make_qkv."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, Sq, D), generator=g, dtype=torch.float32) * q_mult
+    k = torch.randn((B, H, Sk, D), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Sk, D), generator=g, dtype=torch.float32)
+    (qc, dq), (kc, dk), (vc, dv) = (quantize_e4m3(t) for t in (q, k, v))
+    return (qc, kc, vc), (dq, dk, dv)
+
+
 def workload_qkv(index: int):
-    """Inputs of workload ``index`` (0..4) with its own seed."""
+    """bf16 inputs of workload ``index`` with its own seed."""
     w = WORKLOADS[index]
     return make_qkv(w.B, w.H, w.Sq, w.Sk, w.D, SEED_BASE + index, w.q_mult)
+
+
+def workload_qkv_fp8(index: int):
+    """e4m3 inputs (codes, descales) of workload ``index`` with its own seed."""
+    w = WORKLOADS[index]
+    return make_qkv_fp8(w.B, w.H, w.Sq, w.Sk, w.D, SEED_BASE + index, w.q_mult)
+
+
+def u8_codes(t: torch.Tensor) -> np.ndarray:
+    """uint8 numpy copy of a CPU code tensor, for the oracle."""
+    return t.detach().cpu().contiguous().view(torch.uint8).numpy()
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

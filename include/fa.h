@@ -103,6 +103,31 @@ int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *l
                   void *stream);
 
 /*
+ * fa_fwd_fp8 -- attention forward with 8-bit (e4m3) Q, K, V and per-tensor
+ * scaling: the FP8 tensor-core path that "Architectural Innovations in
+ * FlashAttention-2 and FlashAttention-3" names as FA3's throughput lever
+ * (section 三, FA3 item (3)), with the loss of precision held in check by
+ * scaling and mixed precision (section 四, item ③).
+ *
+ * Each of q, k, v is an e4m3 tensor (1 byte per element: sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; 0x7F and 0xFF are NaN) whose real value
+ * is code * descale_x; layouts are fa_fwd's ([B, H, S, D] row-major, device
+ * memory, 16-byte aligned).  The call computes, for the dequantised inputs,
+ *   O   = softmax(scale * Q K^T [+ causal mask]) V   (bf16 [B, H, Sq, D])
+ *   LSE = natural-log row log-sum-exp of scale * Q K^T  (fp32 [B, H, Sq])
+ * S accumulates in fp32; P is rounded to e4m3 (times a power of two) for the
+ * P V product, which accumulates in fp32; O is rounded to bf16 once.
+ * D must be 128.  causal as in fa_fwd (needs Sq == Sk).  Ownership and
+ * launch semantics are fa_fwd's.
+ * Errors: those of fa_fwd; FA_ERR_UNSUPPORTED_D for D != 128;
+ * FA_ERR_BAD_SCALE when scale or a descale is not finite and > 0 (or their
+ * product underflows or overflows fp32).
+ */
+int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int Sq, int Sk, int D, float scale, int causal, float descale_q, float descale_k,
+               float descale_v, void *stream);
+
+/*
  * fa_fwd_splitkv -- attention for decode: a few query rows per head against a
  * long key/value sequence, with the keys of each head split across CTAs.
  * "FlashAttention-2 — L3 Cross-Paper Synthesis", §5 item 5 (decode needs

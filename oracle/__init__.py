@@ -182,6 +182,32 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u32.view(np.float32).astype(np.float64)
 
 
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact value of each e4m3 code (uint8), written from the format's definition
+    in the OCP 8-bit floating point specification: bit 7 sign, bits 6..3 a biased
+    exponent E (bias 7), bits 2..0 a mantissa M.  E = 0 is subnormal,
+    M/8 * 2^-6; otherwise (1 + M/8) * 2^(E-7).  There are no infinities; the two
+    codes with E = 15 and M = 7 (0x7F, 0xFF) are NaN, so 448 is the largest
+    finite magnitude."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    val = np.where((c & 0x80) != 0, -mag, mag)
+    return np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def attn_fwd_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float,
+                 scale: float, causal: bool = False, nthreads: int | None = None, lib=None):
+    """fp64 attention of the dequantised 8-bit inputs: Q = e4m3(q8) * descale_q and
+    likewise K and V (per-tensor scaling), then the materialised forward.  The
+    descales are taken as float32 values, as the kernel receives them.  Returns
+    (O float64 [B,H,Sq,D], LSE float64 [B,H,Sq])."""
+    deq = [e4m3_to_f64(x) * float(np.float32(d))
+           for x, d in ((q8, descale_q), (k8, descale_k), (v8, descale_v))]
+    return attn_fwd(*deq, scale, causal, nthreads=nthreads, lib=lib)
+
+
 def attn_bwd(q, k, v, dout, scale: float, causal: bool = False, window=(-1, -1),
              nthreads: int | None = None, lib=None):
     """Gradients (dQ, dK, dV) of the attention forward for output gradient ``dout``

@@ -171,3 +171,19 @@ def test_bwd_argument_checks():
     assert bcall(scale=float("nan")) == fa.FA_ERR_BAD_SCALE
     assert bcall(ptrs=P[:6] + [P[0] + 16] + P[7:]) == fa.FA_ERR_ALIAS   # dq over q
     assert bcall(ptrs=P[:7] + [P[6]] + P[8:]) == fa.FA_ERR_ALIAS        # dk == dq
+
+
+def test_fp8_argument_checks():
+    def fcall(q=A, D=128, causal=0, Sq=128, Sk=128, scale=0.1, ds=(0.01, 0.01, 0.01), lse=A5,
+              o=A4):
+        return fa.fa_fwd_fp8_raw(q, A2, A3, o, lse, 1, 1, Sq, Sk, D, scale, causal, *ds, 0)
+
+    assert fcall(q=0) == fa.FA_ERR_NULLPTR
+    assert fcall(lse=A5 + 4) == fa.FA_ERR_MISALIGNED
+    assert fcall(D=64) == fa.FA_ERR_UNSUPPORTED_D
+    assert fcall(causal=1, Sk=256) == fa.FA_ERR_UNSUPPORTED_CAUSAL
+    assert fcall(ds=(0.01, 0.0, 0.01)) == fa.FA_ERR_BAD_SCALE
+    assert fcall(ds=(0.01, 0.01, float("inf"))) == fa.FA_ERR_BAD_SCALE
+    assert fcall(ds=(1e-30, 1e-30, 1.0)) == fa.FA_ERR_BAD_SCALE   # product underflows
+    assert fcall(o=A + 8192) == fa.FA_ERR_ALIAS   # O (32 KiB bf16) over 16 KiB of q codes
+    assert fcall(Sq=0) == fa.FA_ERR_BAD_SHAPE

@@ -1,0 +1,146 @@
+"""GPU parity of the 8-bit entry point fa_fwd_fp8 against the fp64 oracle.
+
+The oracle computes exact attention of the dequantised e4m3 inputs.  The
+kernel rounds P to e4m3 before the P V product, so its O differs from exact
+attention by at most
+
+    |dO[i,d]| <= sum_j err_j |V[j,d]| / sum_j P[i,j]  +  2^-8 |O[i,d]|  +  1e-4
+
+with P[i,j] = exp(s_ij - max_j s_ij) and err_j = 2^-4 P[i,j] + min(P[i,j], 2^-16):
+round-to-nearest with 3 mantissa bits is off by at most 2^-4 of a normal
+value; values the kernel holds as e4m3 subnormals (below 2^-12 of its running
+max, itself within a factor 4 of the true max) are off by at most 2^-16; the
+last two terms are the bf16 rounding of O (half an ulp, 2^-8 relative at
+most) and fp32 accumulation / ex2.approx.  The row sum, and so LSE, uses P
+before rounding: |dLSE| <= 1e-3, as for bf16 inputs.  On random inputs the
+errors of the many P terms partly cancel, so the mean error is also held to a
+quarter of the mean bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_82_gb300 as fa
+from exact_attention_82_gb300.inputs import SEED_BASE, WORKLOADS, make_qkv_fp8, u8_codes, \
+    workload_qkv_fp8
+
+pytestmark = pytest.mark.gpu
+
+TOL_LSE = 1e-3
+MEAN_FRACTION = 0.25
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    yield
+    assert fa.fa_device_status() == fa.FA_OK
+
+
+def run_fp8(codes, descales, scale, causal):
+    q, k, v = (t.cuda() for t in codes)
+    o, lse = fa.fa_fwd_fp8(q, k, v, *descales, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def o_bound(codes, descales, scale, causal, o_ref, heads=None):
+    """The bound above, per element, for the heads (flat b*H+h indices) given."""
+    q, k, v = (oracle.e4m3_to_f64(u8_codes(t)) * np.float32(d) for t, d in zip(codes, descales))
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    q, k, v = (x.reshape(B * H, -1, D) for x in (q, k, v))
+    o_ref = o_ref.reshape(B * H, Sq, D)
+    heads = range(B * H) if heads is None else heads
+    out = []
+    for h in heads:
+        s = scale * (q[h] @ k[h].T)
+        if causal:
+            s = np.where(np.arange(Sk)[None, :] <= np.arange(Sq)[:, None], s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        err = 2.0 ** -4 * p + np.minimum(p, 2.0 ** -16)
+        out.append(err @ np.abs(v[h]) / p.sum(axis=1, keepdims=True) +
+                   2.0 ** -8 * np.abs(o_ref[h]) + 1e-4)
+    return np.stack(out)
+
+
+def check(o_gpu, lse_gpu, o_ref, lse_ref, bound, what):
+    d = np.abs(o_gpu - o_ref)
+    dl = np.abs(lse_gpu - lse_ref)
+    assert np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(lse_gpu)), f"{what}: non-finite"
+    ratio = d / bound
+    msg = (f"{what}: max|dO|={d.max():.3e} max|dO|/bound={ratio.max():.3f} "
+           f"mean|dO|={d.mean():.3e} mean bound={bound.mean():.3e} max|dLSE|={dl.max():.3e}")
+    assert ratio.max() <= 1.0, msg
+    assert d.mean() <= MEAN_FRACTION * bound.mean(), msg
+    assert dl.max() <= TOL_LSE, msg
+    return msg
+
+
+def parity(B, H, Sq, Sk, causal, seed, q_mult=1.0, scale=None):
+    codes, ds = make_qkv_fp8(B, H, Sq, Sk, 128, seed, q_mult)
+    scale = 128 ** -0.5 if scale is None else scale
+    og, lg = run_fp8(codes, ds, scale, causal)
+    orf, lrf = oracle.attn_fwd_fp8(*(u8_codes(t) for t in codes), *ds, scale, causal)
+    bound = o_bound(codes, ds, scale, causal, orf).reshape(og.shape)
+    return check(og, lg, orf, lrf, bound, f"fp8 B{B} H{H} Sq{Sq} Sk{Sk} causal{int(causal)}")
+
+
+SHAPES = [(1, 1, 1, 1), (1, 1, 2, 2), (1, 1, 128, 128), (3, 1, 63, 63), (1, 1, 65, 65),
+          (2, 2, 127, 127), (1, 3, 129, 129), (2, 3, 389, 389), (1, 2, 1000, 1000)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_fp8_parity_small(shape, causal):
+    B, H, Sq, Sk = shape
+    parity(B, H, Sq, Sk, causal, seed=5000 + sum(shape))
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 300), (200, 70), (128, 1), (300, 511), (77, 1024)])
+def test_fp8_parity_rectangular(Sq, Sk):
+    parity(2, 2, Sq, Sk, False, seed=Sq * 5 + Sk)
+
+
+def test_fp8_parity_peaky_and_scaled():
+    """Q x4 (peaky rows: the running max moves often) and a large softmax scale."""
+    parity(2, 2, 600, 600, True, seed=91, q_mult=4.0)
+    parity(1, 2, 513, 513, False, seed=92, scale=0.5)
+
+
+def test_fp8_descale_v_is_linear_and_bitwise_repeatable():
+    codes, (dq, dk, dv) = make_qkv_fp8(2, 2, 300, 300, 128, seed=17)
+    o1, l1 = run_fp8(codes, (dq, dk, dv), 0.1, False)
+    o2, l2 = run_fp8(codes, (dq, dk, dv), 0.1, False)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    o4, l4 = run_fp8(codes, (dq, dk, 4 * dv), 0.1, False)   # a power of two: exact
+    np.testing.assert_array_equal(o4, 4 * o1)
+    np.testing.assert_array_equal(l4, l1)
+
+
+@pytest.mark.parametrize("index", [i for i, w in enumerate(WORKLOADS) if w.path == "fp8"],
+                         ids=lambda i: WORKLOADS[i].name)
+def test_fp8_workload_sampled_heads(index):
+    """Full-size workload in the benchmark's launch configuration; three whole heads
+    (first, last, one in the middle) checked against the oracle."""
+    w = WORKLOADS[index]
+    codes, ds = workload_qkv_fp8(index)
+    og, lg = run_fp8(codes, ds, w.scale, w.causal)
+    BH = w.B * w.H
+    heads = [0, BH // 2 + 1, BH - 1]
+    sub = [t.reshape(BH, *t.shape[2:])[heads].unsqueeze(0).contiguous() for t in codes]
+    orf, lrf = oracle.attn_fwd_fp8(*(u8_codes(t) for t in sub), *ds, w.scale, w.causal)
+    bound = o_bound(sub, ds, w.scale, w.causal, orf)
+    og = og.reshape(BH, w.Sq, w.D)[heads]
+    lg = lg.reshape(BH, w.Sq)[heads]
+    check(og, lg, orf[0], lrf[0], bound, w.name)
+
+
+def test_fp8_rejects_bad_arguments():
+    z = torch.zeros(1, 1, 128, 128, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_fp8(z, z, z, 1.0, float("nan"), 1.0)
+    z64 = torch.zeros(1, 1, 128, 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_fp8(z64, z64, z64, 1.0, 1.0, 1.0)
