@@ -34,10 +34,15 @@ METRIC = "fwd attention TFLOP/s & % of GB300 dense BF16 peak (causal FLOPs halve
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["exact_attention_82_gb300/csrc/fa_fwd_kernel.cu",
-                  "exact_attention_82_gb300/csrc/sm103_ptx.cuh",
-                  "exact_attention_82_gb300/csrc/fa_internal.h"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
+_CSRC = "exact_attention_82_gb300/csrc/"
+# the sources each path's kernels are built from (a recorded DRAM-traffic figure is
+# valid only while they are unchanged)
+KERNEL_SOURCES = {
+    "fwd": [_CSRC + "fa_fwd_kernel.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_internal.h"],
+    "bwd": [_CSRC + "fa_bwd.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_internal.h"],
+    "splitkv": [_CSRC + "fa_splitkv.cu", _CSRC + "sm103_ptx.cuh", _CSRC + "fa_internal.h"],
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def parse_args(argv=None):
@@ -57,9 +62,14 @@ def parse_args(argv=None):
     return args
 
 
-def kernel_source_hash() -> str:
+def source_group(path: str) -> str:
+    """Which kernel sources serve a workload path ("fp8" and "fwd" share one kernel)."""
+    return path if path in ("bwd", "splitkv") else "fwd"
+
+
+def kernel_source_hash(group: str = "fwd") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[group]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -74,16 +84,17 @@ def measured_peaks():
         return None, "fallback"
 
 
-def traffic_per_launch(workload_name: str):
-    """DRAM bytes per launch from a committed ncu capture, if it still
-    describes the current kernel source; else None."""
+def traffic_per_launch(w):
+    """DRAM bytes per launch (per step, both kernels, for the backward) from a
+    committed ncu capture, if it still describes the current kernel sources;
+    else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get(workload_name)
-    if not entry or entry.get("kernel_sha256") != kernel_source_hash():
+    entry = rec.get(w.name)
+    if not entry or entry.get("kernel_sha256") != kernel_source_hash(source_group(w.path)):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -274,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
     peak = float(peaks["bf16_tflops"]) if peaks else FALLBACK_PEAK_TFLOPS
     tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
     value = whole_job_tflops(w.flops, world, ms)
-    traffic = traffic_per_launch(w.name)
+    traffic = traffic_per_launch(w)
     if w.path == "splitkv":
         # decode reads each key and value once: bound by HBM bandwidth
         hbm_peak = float(peaks["hbm_gbs"]) if peaks else FALLBACK_HBM_GBS
