@@ -269,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int first0 = J - jhi[0], last0 = J - jlo[0];
             const int first1 = act[1] ? J - jhi[1] : N, last1 = act[1] ? J - jlo[1] : -1;
             bool ok = wait(B_Q_FULL, 0);
-            int npv0 = 0, npv1 = 0;        // P V products issued per sub-tile
-            int sk = 0, sv = 0, svp = 0;   // K stage; V stage of the current and previous tile
-            uint32_t kph = 0, vph = 0, vpph = 0;
+            int npv0 = 0, npv1 = 0;  // P V products issued per sub-tile
+            int sk = 0, sv = 0;      // ring stage of K_it and of V_{it-1}
+            uint32_t kph = 0, vph = 0;
             auto issue_s = [&](uint64_t dq, uint32_t s_tm) {
 #pragma unroll
                 for (int kk = 0; kk < C::S_STEPS; ++kk) {
@@ -282,10 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_ss(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, int npv, int stage, uint32_t phase) -> bool {
-                if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
-                if (!wait(B_V_FULL + stage, phase)) return false;
-                tc_fence_after();
+            // O_t += P_t V for the V stage given; its waits are the caller's
+            auto issue_pv_mma = [&](int t, int npv, int stage) {
                 const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
@@ -297,45 +295,109 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
                                   C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
                 }
-                return true;
             };
-            for (int it = 0; ok && it < N; ++it) {
-                ok = wait(B_K_FULL + sk, kph);
-                if (!ok) break;
-                tc_fence_after();
-                const bool p0 = it >= first0 && it <= last0;
-                const bool p1 = it >= first1 && it <= last1;
-                if (p0) {
-                    issue_s(dq0, tmem);
-                    tc_commit(bar(B_S_FULL + 0));
-                }
-                if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
-                    ok = issue_pv(1, npv1++, svp, vpph);
+            if constexpr (!F8) {
+                // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
+                int svp = 0;          // V stage of the previous tile
+                uint32_t vpph = 0;
+                auto issue_pv = [&](int t, int npv, int stage, uint32_t phase) -> bool {
+                    if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                    if (!wait(B_V_FULL + stage, phase)) return false;
+                    tc_fence_after();
+                    issue_pv_mma(t, npv, stage);
+                    return true;
+                };
+                for (int it = 0; ok && it < N; ++it) {
+                    ok = wait(B_K_FULL + sk, kph);
                     if (!ok) break;
-                    if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
-                    tc_commit(bar(B_V_EMPTY + svp));
+                    tc_fence_after();
+                    const bool p0 = it >= first0 && it <= last0;
+                    const bool p1 = it >= first1 && it <= last1;
+                    if (p0) {
+                        issue_s(dq0, tmem);
+                        tc_commit(bar(B_S_FULL + 0));
+                    }
+                    if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
+                        ok = issue_pv(1, npv1++, svp, vpph);
+                        if (!ok) break;
+                        if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                        tc_commit(bar(B_V_EMPTY + svp));
+                    }
+                    if (p1) {
+                        issue_s(dq1, tmem + 128);
+                        tc_commit(bar(B_S_FULL + 1));
+                    }
+                    tc_commit(bar(B_K_EMPTY + sk));
+                    if (p0) {
+                        ok = issue_pv(0, npv0++, sv, vph);
+                        if (!ok) break;
+                        if (it == last0) tc_commit(bar(B_O_DONE + 0));
+                        if (!p1) tc_commit(bar(B_V_EMPTY + sv));
+                    }
+                    if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                    svp = sv;
+                    vpph = vph;
+                    if (++sv == C::VST) { sv = 0; vph ^= 1u; }
                 }
-                if (p1) {
-                    issue_s(dq1, tmem + 128);
-                    tc_commit(bar(B_S_FULL + 1));
+                if (ok && last1 == N - 1) {
+                    ok = issue_pv(1, npv1, svp, vpph);
+                    if (ok) {
+                        tc_commit(bar(B_O_DONE + 1));
+                        tc_commit(bar(B_V_EMPTY + svp));
+                    }
                 }
-                tc_commit(bar(B_K_EMPTY + sk));
-                if (p0) {
-                    ok = issue_pv(0, npv0++, sv, vph);
-                    if (!ok) break;
-                    if (it == last0) tc_commit(bar(B_O_DONE + 0));
-                    if (!p1) tc_commit(bar(B_V_EMPTY + sv));
-                }
-                if (++sk == C::KST) { sk = 0; kph ^= 1u; }
-                svp = sv;
-                vpph = vph;
-                if (++sv == C::VST) { sv = 0; vph ^= 1u; }
-            }
-            if (ok && last1 == N - 1) {
-                ok = issue_pv(1, npv1, svp, vpph);
-                if (ok) {
-                    tc_commit(bar(B_O_DONE + 1));
-                    tc_commit(bar(B_V_EMPTY + svp));
+            } else {
+                // The same MMA order, grouped into two bursts per step:
+                // [PV0_{j-1}, S0_j] and [PV1_{j-1}, S1_j].  Every wait a burst needs
+                // is taken before it and every commit after it, so each step has two
+                // gaps in the MMA stream instead of four; that pays where MMAs are
+                // short (8-bit: half the tensor time per instruction), while the
+                // 16-bit kernel is faster with the loop above.  Step j = N issues
+                // only the last P V.
+                for (int it = 0; ok && it <= N; ++it) {
+                    const bool pv0 = it - 1 >= first0 && it - 1 <= last0;  // PV0 of tile it-1
+                    const bool s0 = it < N && it >= first0 && it <= last0;
+                    const bool pv1 = it - 1 >= first1 && it - 1 <= last1;
+                    const bool s1 = it < N && it >= first1 && it <= last1;
+                    // ---- burst A: PV0_{it-1}, S0_it
+                    if (pv0) {
+                        ok = wait(B_P_FULL + 0, (uint32_t)npv0 & 1u) && wait(B_V_FULL + sv, vph);
+                        if (!ok) break;
+                    }
+                    if (s0 || s1) {
+                        ok = wait(B_K_FULL + sk, kph);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    if (pv0) issue_pv_mma(0, npv0, sv);
+                    if (s0) issue_s(dq0, tmem);
+                    if (pv0) {
+                        if (it - 1 == last0) tc_commit(bar(B_O_DONE + 0));
+                        if (!pv1) tc_commit(bar(B_V_EMPTY + sv));
+                        ++npv0;
+                    }
+                    if (s0) tc_commit(bar(B_S_FULL + 0));
+                    // ---- burst B: PV1_{it-1}, S1_it
+                    if (pv1) {
+                        ok = wait(B_P_FULL + 1, (uint32_t)npv1 & 1u) && (pv0 || wait(B_V_FULL + sv, vph));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv_mma(1, npv1, sv);
+                    }
+                    if (s1) issue_s(dq1, tmem + 128);
+                    if (pv1) {
+                        if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                        tc_commit(bar(B_V_EMPTY + sv));
+                        ++npv1;
+                    }
+                    if (s1) tc_commit(bar(B_S_FULL + 1));
+                    if (s0 || s1) tc_commit(bar(B_K_EMPTY + sk));
+                    if (it < N) {
+                        if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                    }
+                    if (it >= 1) {
+                        if (++sv == C::VST) { sv = 0; vph ^= 1u; }
+                    }
                 }
             }
             // wind down: every MMA issued here is complete before TMEM is freed
