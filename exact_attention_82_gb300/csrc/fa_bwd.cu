@@ -59,9 +59,9 @@ enum : uint32_t {
     BB_FULL = 1,       // + stage (2): ring tiles loaded
     BB_EMPTY = 3,      // + stage: ring stage free
     BB_X_FULL = 5,     // S and dP computed
-    BB_P_FULL = 6,     // element-wise results written to TMEM (128 arrivals)
-    BB_DONE = 7,       // last accumulation finished
-    BB_DRAIN = 8,
+    BB_DONE = 6,       // last accumulation finished
+    BB_DRAIN = 7,
+    BB_CH_FULL = 8,    // + chunk (4): 32 columns of element-wise results in TMEM (128 arrivals)
 };
 constexpr uint32_t BSLOT_TMEM = 128, BSLOT_ABORT = 132;
 constexpr unsigned long long kBwdDrainNs = 20ull * 1000 * 1000;
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(BB_EMPTY + s), 1);
         }
         mbar_init(bar(BB_X_FULL), 1);
-        mbar_init(bar(BB_P_FULL), 128);
+        for (int c = 0; c < 4; ++c) mbar_init(bar(BB_CH_FULL + c), 128);
         mbar_init(bar(BB_DONE), 1);
         mbar_init(bar(BB_DRAIN), 1);
         *abort_flag = 0u;
@@ -163,13 +163,20 @@ __global__ void __launch_bounds__(192, 1)
                     tc_mma_ss(tmem + C::TM_Y, db + off, dv1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(BB_X_FULL));
-                ok = wait(BB_P_FULL, (uint32_t)it & 1u);
-                if (!ok) break;
-                tc_fence_after();
+                // dQ += dS K chunk by chunk, each 32-key chunk as soon as the
+                // element-wise warps have written it (A = dS in TMEM, B = K MN-major)
+                for (int c = 0; ok && c < 4; ++c) {
+                    ok = wait(BB_CH_FULL + c, (uint32_t)it & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < C::T / 16; ++kk)  // A = dS (bf16 in TMEM), B = K (MN-major)
-                    tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + kk * 8, dk2 + so + ((kk * 2048) >> 4),
-                              C::IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * c + h;
+                        tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + kk * 8, dk2 + so + ((kk * 2048) >> 4),
+                                  C::IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
                 tc_commit(bar(BB_EMPTY + st));
             }
             if (ok) tc_commit(bar(BB_DONE));
@@ -215,9 +222,9 @@ __global__ void __launch_bounds__(192, 1)
             const int col0 = (j_hi - it) * C::T;
             const bool masked = it == 0 && mask_first;
             const int lim = (p.causal ? min(p.Sk, row_g + 1) : p.Sk) - col0;
-            uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
                 uint32_t s[32], dp[32];
                 tmem_ld32(x_tm + c * 32, s);
                 tmem_ld32(y_tm + c * 32, dp);
@@ -233,13 +240,13 @@ __global__ void __launch_bounds__(192, 1)
                         if (!valid_row || (masked && cc >= lim)) pv = 0.f;
                         pr[h] = pv * (__uint_as_float(dp[2 * e + h]) - delta);
                     }
-                    pk[c * 16 + e] = b16_pack(pr[0], pr[1]);
+                    pk[e] = b16_pack(pr[0], pr[1]);
                 }
-                tmem_st16(x_tm + c * 16, &pk[c * 16]);
+                tmem_st16(x_tm + c * 16, pk);
+                tmem_st_wait16(pk);
+                tc_fence_before();
+                mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
             }
-            tmem_st_wait64(pk);
-            tc_fence_before();
-            mbar_arrive(bar(BB_P_FULL));
         }
         // ---- epilogue: dQ = scale * acc -> bf16 -> shared (the Q tile) -> TMA store
         if (ok) ok = wait(BB_DONE, 0);
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(BB_EMPTY + s), 1);
         }
         mbar_init(bar(BB_X_FULL), 1);
-        mbar_init(bar(BB_P_FULL), 128);
+        for (int c = 0; c < 4; ++c) mbar_init(bar(BB_CH_FULL + c), 128);
         mbar_init(bar(BB_DONE), 1);
         mbar_init(bar(BB_DRAIN), 1);
         *abort_flag = 0u;
@@ -381,17 +388,22 @@ __global__ void __launch_bounds__(192, 1)
                     tc_mma_ss(tmem + C::TM_Y, dva + off, do1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(BB_X_FULL));
-                ok = wait(BB_P_FULL, (uint32_t)it & 1u);
-                if (!ok) break;
-                tc_fence_after();
+                // dV += P^T dO (A = P^T over S^T) and dK += dS^T Q (A = dS^T over dP^T),
+                // each 32-query chunk as soon as the element-wise warps have written it
+                for (int c = 0; ok && c < 4; ++c) {
+                    ok = wait(BB_CH_FULL + c, (uint32_t)it & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < C::T / 16; ++kk) {
-                    // dV += P^T dO (A = P^T over S^T), dK += dS^T Q (A = dS^T over dP^T)
-                    tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + kk * 8, do2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
-                              (it > 0 || kk > 0) ? 1u : 0u);
-                    tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + kk * 8, dq2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
-                              (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * c + h;
+                        tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + kk * 8, do2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + kk * 8, dq2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
+                if (!ok) break;
                 tc_commit(bar(BB_EMPTY + st));
             }
             if (ok) tc_commit(bar(BB_DONE));
@@ -422,9 +434,9 @@ __global__ void __launch_bounds__(192, 1)
             if (ok) {
                 tc_fence_after();
                 const bool masked = it == 0 && mask_first;  // diagonal: keys above the query are out
-                uint32_t pk[64], dk[64];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16], dk[16];
                     uint32_t s[32], dp[32];
                     tmem_ld32(x_tm + c * 32, s);
                     tmem_ld32(y_tm + c * 32, dp);
@@ -441,16 +453,16 @@ __global__ void __launch_bounds__(192, 1)
                             pr[h] = pv;
                             ds[h] = pv * (__uint_as_float(dp[2 * e + h]) - lv[128 + cc]);
                         }
-                        pk[c * 16 + e] = b16_pack(pr[0], pr[1]);
-                        dk[c * 16 + e] = b16_pack(ds[0], ds[1]);
+                        pk[e] = b16_pack(pr[0], pr[1]);
+                        dk[e] = b16_pack(ds[0], ds[1]);
                     }
-                    tmem_st16(x_tm + c * 16, &pk[c * 16]);
-                    tmem_st16(y_tm + c * 16, &dk[c * 16]);
+                    tmem_st16(x_tm + c * 16, pk);
+                    tmem_st16(y_tm + c * 16, dk);
+                    tmem_st_wait16(pk);
+                    tmem_st_wait16(dk);
+                    tc_fence_before();
+                    mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
                 }
-                tmem_st_wait64(pk);
-                tmem_st_wait64(dk);
-                tc_fence_before();
-                mbar_arrive(bar(BB_P_FULL));
             }
         }
         // ---- epilogue: dV and scale * dK -> bf16 -> shared (the K and V tiles) -> TMA store
