@@ -102,6 +102,20 @@ extern "C" const char *fa_strerror(int status) {
     return t_errbuf;
 }
 
+// SMs of the current device (cached per device): persistent forward kernels
+// run at most one CTA per SM, and the split-KV heuristic sizes its grid by it.
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 // Checks shared by the forward entry points; FA_OK when the call may launch.
 static int check_fwd(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
                      int Sq, int Sk, int D, float scale) {
@@ -136,7 +150,10 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
         !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
         return fail_cuda(cudaErrorInvalidValue);
     fa::FwdParams p;
+    p.o = o;
     p.lse = lse;
+    p.bh_count = (int)BH;
+    p.n_items = (int)(n_mblk * BH);
     p.Sq = Sq;
     p.Sk = Sk;
     p.n_mblk = (int)n_mblk;
@@ -147,7 +164,7 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.o_scale = 1.f;
     p.timeout_ns = kWaitLimitNs;
-    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, n_mblk * BH, (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
 }
@@ -201,7 +218,10 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
         !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN, 1) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
         return fail_cuda(cudaErrorInvalidValue);
     fa::FwdParams p;
+    p.o = o;
     p.lse = lse;
+    p.bh_count = (int)BH;
+    p.n_items = (int)(n_mblk * BH);
     p.Sq = Sq;
     p.Sk = Sk;
     p.n_mblk = (int)n_mblk;
@@ -212,24 +232,12 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale_log2;
     p.o_scale = descale_v;
     p.timeout_ns = kWaitLimitNs;
-    const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, tm_o, p, n_mblk * BH, (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, tm_o, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
 }
 
 // ------------------------------------------------------------- split-KV path
-static int sm_count() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
-
 // Keys per split for `splits` ranges: a multiple of the 128-key tile.
 static int split_chunk(int Sk, int splits) {
     const int per = (Sk + splits - 1) / splits;

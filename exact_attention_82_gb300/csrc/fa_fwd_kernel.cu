@@ -6,14 +6,20 @@
 // "第二处源码差异：kernel 主循环怎么组织" (running row max m, running sum l,
 // acc rescaled by exp(m - m_new), a single division by l at the end).
 //
-// Mapping onto the chip.  The grid is (query blocks x batch x heads), the
-// launch shape of the same page's section "第一处源码差异：launch grid 怎么铺";
-// each CTA owns 256 query rows as two 128-row sub-tiles t = 0, 1, which share
-// every K/V tile:
+// Mapping onto the chip.  The work items are the (query block, batch x head)
+// pairs of the same page's launch grid (section "第一处源码差异：launch grid
+// 怎么铺"); the kernel is persistent: one CTA per SM takes one item per round
+// of gridDim.x items, in snake order (causal: all heads' longest query
+// blocks first).  TMEM is allocated and the barriers initialised once, and the next
+// item's Q and first K/V tiles load while the current item finishes, which
+// takes the fixed cost of a CTA (launch, setup, load latency, epilogue) off
+// every item but the first.  Each item is 256 query rows as two 128-row
+// sub-tiles t = 0, 1, which share every K/V tile:
 //   warps 10-11 idle (they complete the third warpgroup, whose registers go
 //              to the softmax warpgroups);
-//   warp 9     TMA producer: Q0 and Q1 once, then K_j and V_j into two
-//              shared-memory rings (128-byte swizzle), K kept one tile ahead;
+//   warp 9     TMA producer: Q0 and Q1 of each item (as soon as the previous
+//              item's last S MMA has read the buffer), then K_j and V_j into
+//              two shared-memory rings (128-byte swizzle), K one tile ahead;
 //   warp 8     allocates all 512 tensor-memory (TMEM) columns and issues the
 //              tcgen05 MMAs from one thread, in the order
 //                S0_j = Q0 K_j^T,  O1 += P1_{j+1} V_{j+1},  S1_j = Q1 K_j^T,
@@ -25,7 +31,9 @@
 //              (only on its first key tile), updates the running max and sum,
 //              writes P (bf16) back over its S row in TMEM, where the P V MMA
 //              reads it as its A operand, and at the end scales O by 1/l,
-//              stages it in shared memory for a TMA store and writes LSE.
+//              writes its O row (a persistent CTA to global memory directly;
+//              a CTA with one item through shared memory and a TMA store)
+//              and LSE.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
 // the first 64 columns of S_t (128 bf16 packed in pairs).
 //
@@ -64,18 +72,14 @@ struct FwdCfg {
     static constexpr int VST = (F8 || D == 64) ? 4 : 2;
     static constexpr int NCH = D * EB / 128;              // 128-byte column chunks per Q/K/V row
     static constexpr int CH_ELEMS = 128 / EB;             // elements per chunk
-    static constexpr int O_NCH = D / 64;                  // 128-byte chunks per bf16 O row
     static constexpr uint32_t QT_BYTES = BM * D * EB;     // one query sub-tile
     static constexpr uint32_t KV_BYTES = BN * D * EB;     // one K or V tile
-    static constexpr uint32_t OT_BYTES = BM * D * 2;      // one bf16 output sub-tile
     static constexpr uint32_t CHUNK = 128 * 128;          // 128 rows x 128 bytes
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
-    // bf16 stages O in its own (then free) Q buffer; an 8-bit one is too small
-    static constexpr uint32_t OFF_O = F8 ? OFF_V + VST * KV_BYTES : OFF_Q;
-    static constexpr uint32_t OFF_BAR = F8 ? OFF_O + 2 * OT_BYTES : OFF_V + VST * KV_BYTES;
-    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
+    static constexpr uint32_t BAR_BYTES = 384;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256;
@@ -88,7 +92,7 @@ struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(!F8 || D == 128, "8-bit rows must fill one 128-byte swizzle atom");
     static_assert(BM == 128 && BN == 128, "tile");
-    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_O % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(SMEM > 114 * 1024, "one CTA per SM (it takes all TMEM columns)");
 };
@@ -103,31 +107,87 @@ constexpr float kF8Lazy = 2.f;
 
 // barrier slots (8 bytes each) inside the OFF_BAR block
 enum : uint32_t {
-    B_Q_FULL = 0,
-    B_K_FULL = 1,    // + stage (up to 4)
-    B_K_EMPTY = 5,   // + stage
-    B_V_FULL = 9,    // + stage
-    B_V_EMPTY = 13,  // + stage
-    B_S_FULL = 17,   // + sub-tile
-    B_P_FULL = 19,   // + sub-tile
-    B_O_DONE = 21,   // + sub-tile
-    B_DRAIN = 23,
+    B_Q_FULL = 0,    // + sub-tile: Q_t of the current item loaded
+    B_Q_FREE = 2,    // + sub-tile: the item's last S_t has read Q_t
+    B_K_FULL = 4,    // + stage (up to 4)
+    B_K_EMPTY = 8,   // + stage
+    B_V_FULL = 12,   // + stage
+    B_V_EMPTY = 16,  // + stage
+    B_S_FULL = 20,   // + sub-tile
+    B_P_FULL = 22,   // + sub-tile
+    B_O_DONE = 24,   // + sub-tile: the item's last P_t V is complete
+    B_O_FREE = 26,   // + sub-tile: the softmax warps have read O_t out (128 arrivals)
+    B_DRAIN = 28,
 };
-constexpr uint32_t SLOT_TMEM = 200;   // byte offset of the TMEM base address
-constexpr uint32_t SLOT_ABORT = 204;  // byte offset of the abort flag
+constexpr uint32_t SLOT_TMEM = 320;   // byte offset of the TMEM base address
+constexpr uint32_t SLOT_ABORT = 324;  // byte offset of the abort flag
 constexpr unsigned long long kDrainNs = 20ull * 1000 * 1000;  // 20 ms
 constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+2 idle)
 // Register split.  At launch every thread has 168 (3 warps per SM sub-partition);
-// the MMA/TMA warpgroup drops to 72 and the softmax warpgroups rise to 216:
-// 256 x 216 + 128 x 72 = 64512 = 384 x 168, the block's launch total.
-constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 72;
+// the MMA/TMA warpgroup drops to 104 and the softmax warpgroups rise to 200:
+// 256 x 200 + 128 x 104 = 64512 = 384 x 168, the block's launch total.  Both
+// sides then compile without spills (the MMA thread's loop is the critical path).
+constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
+
+// One work item: 256 query rows (two sub-tiles) of one (batch, head), and the
+// key tiles [jlo_t, jhi_t] each sub-tile needs.  Key tiles are loaded from J
+// down to J - N + 1; sub-tile t takes part in load-order tiles first_t..last_t.
+struct Item {
+    int bh, row0;
+    bool act1;  // sub-tile 1 has rows (sub-tile 0 always has)
+    int jhi[2], jlo[2];
+    int J, N;
+    int first[2], last[2];
+};
+
+// The r-th item of this CTA: items are dealt out in rounds of gridDim.x in
+// snake order (CTA b takes r G + b in even rounds, r G + G - 1 - b in odd
+// ones), which evens out the CTAs' totals when items come longest first.
+// Past the last item: a value >= p.n_items, and every later round's too.
+__device__ __forceinline__ int item_index(int r) {
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    return r * G + ((r & 1) ? G - 1 - b : b);
+}
+
+template <bool WIN>
+__device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
+    Item g;
+    int mi;
+    if (p.causal) {  // all heads' longest query blocks first
+        mi = k / p.bh_count;
+        g.bh = k - mi * p.bh_count;
+    } else {
+        g.bh = k / p.n_mblk;
+        mi = k - g.bh * p.n_mblk;
+    }
+    const int mblk = p.causal ? (p.n_mblk - 1 - mi) : mi;
+    g.row0 = mblk * kCtaRows;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r_first = g.row0 + t * kBlockM, r_last = r_first + kBlockM - 1;
+        g.jhi[t] = p.n_kv - 1;
+        if (p.wr >= 0) g.jhi[t] = min(g.jhi[t], (r_last + p.wr) / kBlockN);
+        g.jlo[t] = (WIN && p.wl >= 0) ? max(0, (r_first - p.wl) / kBlockN) : 0;
+    }
+    g.act1 = g.row0 + kBlockM < p.Sq;
+    g.J = g.act1 ? max(g.jhi[0], g.jhi[1]) : g.jhi[0];
+    g.N = g.J - g.jlo[0] + 1;  // sub-tile 0 reaches lowest
+    g.first[0] = g.J - g.jhi[0];
+    g.last[0] = g.J - g.jlo[0];
+    g.first[1] = g.act1 ? g.J - g.jhi[1] : g.N;
+    g.last[1] = g.act1 ? g.J - g.jlo[1] : -1;
+    return g;
+}
 
 // WIN: a bounded key band (window_left >= 0 or window_right > 0).  Without it
 // (full or causal attention) only a sub-tile's first key tile can need a mask
 // and every row has an allowed key in it, which the code below exploits.
 // F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
-template <int D, bool WIN, bool F8>
+// PERSIST: the grid may be smaller than the item count, so a CTA walks items
+// and hands Q and O buffers over between them; without it every CTA has one
+// item and the hand-over code is compiled out of the MMA thread's loop.
+template <int D, bool WIN, bool F8, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -142,26 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- which tile: blockIdx.x = bh * n_mblk + (query-block order)
-    const int mi = (int)(blockIdx.x % (unsigned)p.n_mblk);
-    const int bh = (int)(blockIdx.x / (unsigned)p.n_mblk);
-    const int mblk = p.causal ? (p.n_mblk - 1 - mi) : mi;  // causal: longest first
-    const int row0 = mblk * 2 * C::BM;
-    // key tiles [jlo, jhi] a sub-tile needs: those meeting some row's window
-    bool act[2];
-    int jhi[2], jlo[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int r_first = row0 + t * C::BM, r_last = r_first + C::BM - 1;
-        act[t] = r_first < p.Sq;
-        jhi[t] = p.n_kv - 1;
-        if (p.wr >= 0) jhi[t] = min(jhi[t], (r_last + p.wr) / C::BN);
-        jlo[t] = (WIN && p.wl >= 0) ? max(0, (r_first - p.wl) / C::BN) : 0;
-    }
-    const int J = act[1] ? max(jhi[0], jhi[1]) : jhi[0];  // first key tile of the CTA
-    const int J_lo = jlo[0];                              // sub-tile 0 reaches lowest
-    const int N = J - J_lo + 1;                           // key tiles the CTA loads
-
     const uint32_t sQ = sbase + C::OFF_Q;
     const uint32_t sK = sbase + C::OFF_K;
     const uint32_t sV = sbase + C::OFF_V;
@@ -171,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + SLOT_TMEM);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q_FULL), 1);
         for (int s = 0; s < C::KST; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
@@ -181,9 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_Q_FULL + t), 1);
+            mbar_init(bar(B_Q_FREE + t), 1);
             mbar_init(bar(B_S_FULL + t), 1);
             mbar_init(bar(B_P_FULL + t), 128);
             mbar_init(bar(B_O_DONE + t), 1);
+            mbar_init(bar(B_O_FREE + t), 128);
         }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0u;
@@ -214,191 +256,264 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_map(&tm_v);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(B_Q_FULL), (act[1] ? 2u : 1u) * C::QT_BYTES);
-            for (int t = 0; t < 2; ++t)
-                if (act[t])
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS, row0 + t * C::BM, bh,
-                                    bar(B_Q_FULL), pol_q);
-            int nk = 0, nv = 0;  // loads issued
-            auto load_k = [&](int it) -> bool {
-                const int st = it % C::KST;
-                if (!wait(B_K_EMPTY + st, ((uint32_t)(it / C::KST) & 1u) ^ 1u)) return false;
+            int nk = 0, nv = 0;      // K and V tiles loaded so far (ring positions), over all items
+            int qn0 = 0, qn1 = 0;    // Q_0 and Q_1 loads so far
+            bool ok = true;
+            auto load_k = [&](const Item &g, int it) -> bool {
+                const int st = nk % C::KST;
+                if (!wait(B_K_EMPTY + st, ((uint32_t)(nk / C::KST) & 1u) ^ 1u)) return false;
                 mbar_arrive_expect_tx(bar(B_K_FULL + st), C::KV_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tm_k, c * C::CH_ELEMS, (J - it) * C::BN, bh,
-                                bar(B_K_FULL + st), pol_kv);
-                nk = it + 1;
+                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tm_k, c * C::CH_ELEMS, (g.J - it) * C::BN,
+                                g.bh, bar(B_K_FULL + st), pol_kv);
+                ++nk;
                 return true;
             };
-            auto load_v = [&](int it) -> bool {
-                const int st = it % C::VST;
-                if (!wait(B_V_EMPTY + st, ((uint32_t)(it / C::VST) & 1u) ^ 1u)) return false;
+            auto load_v = [&](const Item &g, int it) -> bool {
+                const int st = nv % C::VST;
+                if (!wait(B_V_EMPTY + st, ((uint32_t)(nv / C::VST) & 1u) ^ 1u)) return false;
                 mbar_arrive_expect_tx(bar(B_V_FULL + st), C::KV_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tm_v, c * C::CH_ELEMS, (J - it) * C::BN, bh,
-                                bar(B_V_FULL + st), pol_kv);
-                nv = it + 1;
+                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tm_v, c * C::CH_ELEMS, (g.J - it) * C::BN,
+                                g.bh, bar(B_V_FULL + st), pol_kv);
+                ++nv;
                 return true;
             };
-            bool ok = load_k(0);
-            for (int it = 0; ok && it < N; ++it) {
-                if (it + 1 < N) ok = load_k(it + 1);
-                if (ok) ok = load_v(it);
+            for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
+                const Item g = item_at<WIN>(p, k);
+                // Q_t of this item, once the previous item's last S_t has read the buffer
+                auto load_q = [&](int t, int &qn) -> bool {
+                    if (qn > 0 && !wait(B_Q_FREE + t, (uint32_t)(qn - 1) & 1u)) return false;
+                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), C::QT_BYTES);
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS, g.row0 + t * C::BM,
+                                    g.bh, bar(B_Q_FULL + t), pol_q);
+                    ++qn;
+                    return true;
+                };
+                ok = load_q(0, qn0) && (!g.act1 || load_q(1, qn1));
+                if (ok) ok = load_k(g, 0);
+                for (int it = 0; ok && it < g.N; ++it) {
+                    if (it + 1 < g.N) ok = load_k(g, it + 1);
+                    if (ok) ok = load_v(g, it);
+                }
             }
             // wind down: every copy issued here has landed before the CTA may exit
-            mbar_wait_drain(bar(B_Q_FULL), 0, kDrainNs);
-            for (int it = (nk > C::KST ? nk - C::KST : 0); it < nk; ++it)
-                mbar_wait_drain(bar(B_K_FULL + it % C::KST), (uint32_t)(it / C::KST) & 1u, kDrainNs);
-            for (int it = (nv > C::VST ? nv - C::VST : 0); it < nv; ++it)
-                mbar_wait_drain(bar(B_V_FULL + it % C::VST), (uint32_t)(it / C::VST) & 1u, kDrainNs);
+            if (qn0 > 0) mbar_wait_drain(bar(B_Q_FULL + 0), (uint32_t)(qn0 - 1) & 1u, kDrainNs);
+            if (qn1 > 0) mbar_wait_drain(bar(B_Q_FULL + 1), (uint32_t)(qn1 - 1) & 1u, kDrainNs);
+            for (int i = (nk > C::KST ? nk - C::KST : 0); i < nk; ++i)
+                mbar_wait_drain(bar(B_K_FULL + i % C::KST), (uint32_t)(i / C::KST) & 1u, kDrainNs);
+            for (int i = (nv > C::VST ? nv - C::VST : 0); i < nv; ++i)
+                mbar_wait_drain(bar(B_V_FULL + i % C::VST), (uint32_t)(i / C::VST) & 1u, kDrainNs);
         }
     } else if (warp == 8) {
         // ======================================================= MMA issuer
         regs_decrease<kRegsOther>();
         if (lane == 0) {
-            // This thread is on the critical path of every tile, so its loop is
-            // kept lean: descriptors are a 64-bit base plus compile-time offsets
-            // (the start-address field cannot carry: shared addresses < 256 KB),
-            // ring stages and phases advance incrementally, and participation is
-            // a precomputed iteration range per sub-tile.
+            // Issuing one tcgen05.mma takes this thread almost as long as a
+            // 128x128x16 MMA takes to run, so the thread is on the critical
+            // path of every tile and its loop is kept lean: descriptors are a
+            // 64-bit base plus compile-time offsets (the start-address field
+            // cannot carry: shared addresses < 256 KB), ring stages and phases
+            // advance incrementally, and participation is a precomputed
+            // iteration range per sub-tile.
             const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
             const uint64_t dq1 = sw128_desc(sQ + C::QT_BYTES, 16, 1024);
             const uint64_t dk = sw128_desc(sK, 16, 1024);
             const uint64_t dv = sw128_desc(sV, C::CHUNK, 1024);
-            const int first0 = J - jhi[0], last0 = J - jlo[0];
-            const int first1 = act[1] ? J - jhi[1] : N, last1 = act[1] ? J - jlo[1] : -1;
-            bool ok = wait(B_Q_FULL, 0);
-            int npv0 = 0, npv1 = 0;  // P V products issued per sub-tile
-            int sk = 0, sv = 0;      // ring stage of K_it and of V_{it-1}
+            int sk = 0, sv = 0;       // ring stage of the next K and V tile to be read, over all items
             uint32_t kph = 0, vph = 0;
-            auto issue_s = [&](uint64_t dq, uint32_t s_tm) {
+            int qn0 = 0, qn1 = 0;     // items so far in which sub-tile 0 / 1 took part
+            int npv0 = 0, npv1 = 0;   // P V products so far per sub-tile (P_FULL phases)
+            bool ok = true;
+            auto issue_s = [&](uint64_t dq, uint32_t s_tm, int stage) {
+                const uint64_t dks = dk + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::S_STEPS; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
                     if constexpr (F8)
-                        tc_mma_ss_f8(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+                        tc_mma_ss_f8(s_tm, dq + off, dks + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                     else
-                        tc_mma_ss(s_tm, dq + off, dk + ((sk * C::KV_BYTES) >> 4) + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+                        tc_mma_ss(s_tm, dq + off, dks + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            // O_t += P_t V for the V stage given; its waits are the caller's
-            auto issue_pv_mma = [&](int t, int npv, int stage) {
+            // O_t += P_t V (the item's first product overwrites O_t); its waits are the caller's
+            auto issue_pv_mma = [&](int t, bool accumulate, int stage) {
                 const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                     // A = P_t in TMEM (8 columns = 32 bytes of keys per step); B = V, MN-major
+                    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
                     if constexpr (F8)
                         tc_mma_ts_f8(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
-                                     C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
+                                     C::IDESC_PV, acc);
                     else
                         tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
-                                  C::IDESC_PV, (npv > 0 || kk > 0) ? 1u : 0u);
+                                  C::IDESC_PV, acc);
                 }
             };
-            if constexpr (!F8) {
-                // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
-                int svp = 0;          // V stage of the previous tile
-                uint32_t vpph = 0;
-                auto issue_pv = [&](int t, int npv, int stage, uint32_t phase) -> bool {
-                    if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
-                    if (!wait(B_V_FULL + stage, phase)) return false;
-                    tc_fence_after();
-                    issue_pv_mma(t, npv, stage);
-                    return true;
-                };
-                for (int it = 0; ok && it < N; ++it) {
-                    ok = wait(B_K_FULL + sk, kph);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const bool p0 = it >= first0 && it <= last0;
-                    const bool p1 = it >= first1 && it <= last1;
-                    if (p0) {
-                        issue_s(dq0, tmem);
-                        tc_commit(bar(B_S_FULL + 0));
-                    }
-                    if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
-                        ok = issue_pv(1, npv1++, svp, vpph);
-                        if (!ok) break;
-                        if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
-                        tc_commit(bar(B_V_EMPTY + svp));
-                    }
-                    if (p1) {
-                        issue_s(dq1, tmem + 128);
-                        tc_commit(bar(B_S_FULL + 1));
-                    }
-                    tc_commit(bar(B_K_EMPTY + sk));
-                    if (p0) {
-                        ok = issue_pv(0, npv0++, sv, vph);
-                        if (!ok) break;
-                        if (it == last0) tc_commit(bar(B_O_DONE + 0));
-                        if (!p1) tc_commit(bar(B_V_EMPTY + sv));
-                    }
-                    if (++sk == C::KST) { sk = 0; kph ^= 1u; }
-                    svp = sv;
-                    vpph = vph;
-                    if (++sv == C::VST) { sv = 0; vph ^= 1u; }
-                }
-                if (ok && last1 == N - 1) {
-                    ok = issue_pv(1, npv1, svp, vpph);
-                    if (ok) {
-                        tc_commit(bar(B_O_DONE + 1));
-                        tc_commit(bar(B_V_EMPTY + svp));
-                    }
-                }
-            } else {
-                // The same MMA order, grouped into two bursts per step:
-                // [PV0_{j-1}, S0_j] and [PV1_{j-1}, S1_j].  Every wait a burst needs
-                // is taken before it and every commit after it, so each step has two
-                // gaps in the MMA stream instead of four; that pays where MMAs are
-                // short (8-bit: half the tensor time per instruction), while the
-                // 16-bit kernel is faster with the loop above.  Step j = N issues
-                // only the last P V.
-                for (int it = 0; ok && it <= N; ++it) {
-                    const bool pv0 = it - 1 >= first0 && it - 1 <= last0;  // PV0 of tile it-1
-                    const bool s0 = it < N && it >= first0 && it <= last0;
-                    const bool pv1 = it - 1 >= first1 && it - 1 <= last1;
-                    const bool s1 = it < N && it >= first1 && it <= last1;
-                    // ---- burst A: PV0_{it-1}, S0_it
-                    if (pv0) {
-                        ok = wait(B_P_FULL + 0, (uint32_t)npv0 & 1u) && wait(B_V_FULL + sv, vph);
-                        if (!ok) break;
-                    }
-                    if (s0 || s1) {
+            // before an item's first S_t: its Q_t has landed
+            auto q_ready = [&](int t) { return wait(B_Q_FULL + t, (uint32_t)(t ? qn1 : qn0) & 1u); };
+            // before an item's first P_t V: the softmax warps have read the previous item's O_t
+            auto o_free = [&](int t) {
+                const int q = t ? qn1 : qn0;
+                return q == 0 || wait(B_O_FREE + t, (uint32_t)(q - 1) & 1u);
+            };
+            for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
+                const Item g = item_at<WIN>(p, k);
+                const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
+                const int N = g.N;
+                int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
+                if constexpr (!F8) {
+                    // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
+                    int svp = 0;          // V stage of the previous tile
+                    uint32_t vpph = 0;
+                    auto issue_pv = [&](int t, int ipv, int stage, uint32_t phase) -> bool {
+                        int &npv = t ? npv1 : npv0;
+                        if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                        if (!wait(B_V_FULL + stage, phase)) return false;
+                        if constexpr (PERSIST) {
+                            if (ipv == 0 && !o_free(t)) return false;
+                        }
+                        tc_fence_after();
+                        issue_pv_mma(t, ipv > 0, stage);
+                        ++npv;
+                        return true;
+                    };
+                    if constexpr (!PERSIST) ok = q_ready(0) && (!g.act1 || q_ready(1));
+                    for (int it = 0; ok && it < N; ++it) {
                         ok = wait(B_K_FULL + sk, kph);
                         if (!ok) break;
-                    }
-                    tc_fence_after();
-                    if (pv0) issue_pv_mma(0, npv0, sv);
-                    if (s0) issue_s(dq0, tmem);
-                    if (pv0) {
-                        if (it - 1 == last0) tc_commit(bar(B_O_DONE + 0));
-                        if (!pv1) tc_commit(bar(B_V_EMPTY + sv));
-                        ++npv0;
-                    }
-                    if (s0) tc_commit(bar(B_S_FULL + 0));
-                    // ---- burst B: PV1_{it-1}, S1_it
-                    if (pv1) {
-                        ok = wait(B_P_FULL + 1, (uint32_t)npv1 & 1u) && (pv0 || wait(B_V_FULL + sv, vph));
-                        if (!ok) break;
                         tc_fence_after();
-                        issue_pv_mma(1, npv1, sv);
-                    }
-                    if (s1) issue_s(dq1, tmem + 128);
-                    if (pv1) {
-                        if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
-                        tc_commit(bar(B_V_EMPTY + sv));
-                        ++npv1;
-                    }
-                    if (s1) tc_commit(bar(B_S_FULL + 1));
-                    if (s0 || s1) tc_commit(bar(B_K_EMPTY + sk));
-                    if (it < N) {
+                        const bool p0 = it >= first0 && it <= last0;
+                        const bool p1 = it >= first1 && it <= last1;
+                        if (p0) {
+                            if constexpr (PERSIST) {
+                                if (it == first0) {
+                                    ok = q_ready(0);
+                                    if (!ok) break;
+                                    tc_fence_after();
+                                }
+                            }
+                            issue_s(dq0, tmem, sk);
+                            tc_commit(bar(B_S_FULL + 0));
+                            if constexpr (PERSIST) {
+                                if (it == last0) tc_commit(bar(B_Q_FREE + 0));
+                            }
+                        }
+                        if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
+                            ok = issue_pv(1, ipv1++, svp, vpph);
+                            if (!ok) break;
+                            if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                            tc_commit(bar(B_V_EMPTY + svp));
+                        }
+                        if (p1) {
+                            if constexpr (PERSIST) {
+                                if (it == first1) {
+                                    ok = q_ready(1);
+                                    if (!ok) break;
+                                    tc_fence_after();
+                                }
+                            }
+                            issue_s(dq1, tmem + 128, sk);
+                            tc_commit(bar(B_S_FULL + 1));
+                            if constexpr (PERSIST) {
+                                if (it == last1) tc_commit(bar(B_Q_FREE + 1));
+                            }
+                        }
+                        tc_commit(bar(B_K_EMPTY + sk));
+                        if (p0) {
+                            ok = issue_pv(0, ipv0++, sv, vph);
+                            if (!ok) break;
+                            if (it == last0) tc_commit(bar(B_O_DONE + 0));
+                            if (!p1) tc_commit(bar(B_V_EMPTY + sv));
+                        }
                         if (++sk == C::KST) { sk = 0; kph ^= 1u; }
-                    }
-                    if (it >= 1) {
+                        svp = sv;
+                        vpph = vph;
                         if (++sv == C::VST) { sv = 0; vph ^= 1u; }
                     }
+                    if (ok && last1 == N - 1) {
+                        ok = issue_pv(1, ipv1, svp, vpph);
+                        if (ok) {
+                            tc_commit(bar(B_O_DONE + 1));
+                            tc_commit(bar(B_V_EMPTY + svp));
+                        }
+                    }
+                } else {
+                    // The same MMA order, grouped into two bursts per step:
+                    // [PV0_{j-1}, S0_j] and [PV1_{j-1}, S1_j].  Every wait a burst
+                    // needs is taken before it and every commit after it, so each
+                    // step has two gaps in the MMA stream instead of four; that
+                    // pays where MMAs are short (8-bit: half the tensor time per
+                    // instruction), while the 16-bit kernel is faster with the
+                    // loop above.  Step j = N issues only the last P V.
+                    for (int it = 0; ok && it <= N; ++it) {
+                        const bool pv0 = it - 1 >= first0 && it - 1 <= last0;  // PV0 of tile it-1
+                        const bool s0 = it < N && it >= first0 && it <= last0;
+                        const bool pv1 = it - 1 >= first1 && it - 1 <= last1;
+                        const bool s1 = it < N && it >= first1 && it <= last1;
+                        // ---- burst A: PV0_{it-1}, S0_it
+                        if (pv0) {
+                            ok = wait(B_P_FULL + 0, (uint32_t)npv0 & 1u) && wait(B_V_FULL + sv, vph) &&
+                                 (ipv0 > 0 || o_free(0));
+                            if (!ok) break;
+                        }
+                        if (s0 || s1) {
+                            ok = wait(B_K_FULL + sk, kph);
+                            if (!ok) break;
+                        }
+                        if (s0 && it == first0) {
+                            ok = q_ready(0);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        if (pv0) issue_pv_mma(0, ipv0 > 0, sv);
+                        if (s0) issue_s(dq0, tmem, sk);
+                        if (pv0) {
+                            if (it - 1 == last0) tc_commit(bar(B_O_DONE + 0));
+                            if (!pv1) tc_commit(bar(B_V_EMPTY + sv));
+                            ++npv0;
+                            ++ipv0;
+                        }
+                        if (s0) {
+                            tc_commit(bar(B_S_FULL + 0));
+                            if (it == last0) tc_commit(bar(B_Q_FREE + 0));
+                        }
+                        // ---- burst B: PV1_{it-1}, S1_it
+                        if (pv1) {
+                            ok = wait(B_P_FULL + 1, (uint32_t)npv1 & 1u) && (pv0 || wait(B_V_FULL + sv, vph)) &&
+                                 (ipv1 > 0 || o_free(1));
+                            if (!ok) break;
+                        }
+                        if (s1 && it == first1) {
+                            ok = q_ready(1);
+                            if (!ok) break;
+                        }
+                        if (pv1 || (s1 && it == first1)) tc_fence_after();
+                        if (pv1) issue_pv_mma(1, ipv1 > 0, sv);
+                        if (s1) issue_s(dq1, tmem + 128, sk);
+                        if (pv1) {
+                            if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                            tc_commit(bar(B_V_EMPTY + sv));
+                            ++npv1;
+                            ++ipv1;
+                        }
+                        if (s1) {
+                            tc_commit(bar(B_S_FULL + 1));
+                            if (it == last1) tc_commit(bar(B_Q_FREE + 1));
+                        }
+                        if (s0 || s1) tc_commit(bar(B_K_EMPTY + sk));
+                        if (it < N) {
+                            if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                        }
+                        if (it >= 1) {
+                            if (++sv == C::VST) { sv = 0; vph ^= 1u; }
+                        }
+                    }
                 }
+                ++qn0;
+                if (g.act1) ++qn1;
             }
             // wind down: every MMA issued here is complete before TMEM is freed
             tc_commit(bar(B_DRAIN));
@@ -407,27 +522,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ============================================ softmax warpgroups
         regs_increase<kRegsSoftmax>();
-        const int t = warp >> 2;          // sub-tile
-        const bool my_act = t ? act[1] : act[0];
-        const int my_jhi = t ? jhi[1] : jhi[0];
-        const int my_jlo = t ? jlo[1] : jlo[0];
-        const int r_first = row0 + t * C::BM, r_last = r_first + C::BM - 1;
+        const int t = warp >> 2;            // sub-tile
         const int row = threadIdx.x & 127;  // row in the sub-tile == TMEM lane
-        const int row_g = row0 + t * C::BM + row;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + t * 128;
         const uint32_t o_tm = tmem + lane_off + C::TM_O + t * D;
         const float sl2 = p.scale_log2;
+        int ns = 0;  // S_t tiles so far, over all items (S_FULL phases)
+        int od = 0;  // items so far in which this sub-tile took part (O_DONE phases)
+        // With one item per CTA (not PERSIST) and 16-bit inputs, O is staged in this sub-tile's Q buffer, free once the
+        // item's MMAs are done, and written by a TMA store after the loop;
+        // a persistent CTA stores each row directly, so that its Q buffer
+        // can take the next item's Q as early as possible.
+        constexpr bool tma_epilogue = !F8 && !PERSIST;
+        bool ok = true, staged = false;
+        Item g;
         float m_used = -INFINITY;  // max in exp2 units (raw score * scale*log2e) used for P
         float l_run = 0.f;         // sum of P over the keys seen, relative to m_used
-        bool ok = true;
-        if (my_act) {
+        for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
+            g = item_at<WIN>(p, k);
+            if (t == 1 && !g.act1) continue;
+            const int my_jhi = t ? g.jhi[1] : g.jhi[0], my_jlo = t ? g.jlo[1] : g.jlo[0];
+            const int r_first = g.row0 + t * C::BM, r_last = r_first + C::BM - 1;
+            const int row_g = r_first + row;
             const int n_t = my_jhi - my_jlo + 1;
             // allowed keys of this row: [k_lo, k_hi)
             const int k_lo = (p.wl >= 0) ? row_g - p.wl : 0;
             const int k_hi = (p.wr >= 0) ? min(p.Sk, row_g + p.wr + 1) : p.Sk;
+            m_used = -INFINITY;
+            l_run = 0.f;
             for (int i = 0; i < n_t; ++i) {
-                ok = wait(B_S_FULL + t, (uint32_t)i & 1u);
+                ok = wait(B_S_FULL + t, (uint32_t)ns & 1u);
+                ++ns;
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -598,51 +724,85 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(bar(B_P_FULL + t));
             }
-            if (ok) {
-                ok = wait(B_O_DONE + t, 0);
-                ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait(B_O_DONE + t, (uint32_t)od & 1u));
+            ++od;
+            if (!ok) break;
+            if constexpr (tma_epilogue) {  // the only item of this CTA: epilogue below
+                staged = true;
+                break;
             }
-        }
-        // ---- epilogue: O / l -> bf16 -> shared memory (this sub-tile's Q
-        // buffer, free once its last MMA is done) -> TMA store; LSE.  Both
-        // named barriers run whatever `ok` says, so no warp can be left waiting.
-        named_bar_sync(1 + t, 128);
-        const uint32_t sO = sbase + C::OFF_O + t * C::OT_BYTES;
-        if (my_act && ok) {
+            // ---- epilogue: O_t out of TMEM (after which the next item may
+            // overwrite it), O / l -> bf16 -> this row of O in global memory; LSE
             tc_fence_after();
-            // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
-            const float inv_l = (F8 ? p.o_scale : 1.f) / l_run;
+            uint32_t o[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(o_tm + c * 32, o);
-                tmem_ld_wait(o);
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, o[c]);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int U = c * 4 + u;  // 16-byte unit (8 columns) of the row
-                    uint32_t w[4];
+            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+            tc_fence_before();
+            mbar_arrive(bar(B_O_FREE + t));
+            if (row_g < p.Sq) {
+                // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
+                const float inv_l = (F8 ? p.o_scale : 1.f) / l_run;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
+                                                       ((size_t)g.bh * p.Sq + row_g) * D);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv_l,
-                                           __uint_as_float(o[u * 8 + 2 * e + 1]) * inv_l);
-                    const uint32_t addr = sO + (U >> 3) * C::CHUNK + row * 128 +
-                                          ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
-                    st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-                }
+                for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {  // 16-byte unit (8 columns) c * 4 + u of the row
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(o[c][u * 8 + 2 * e]) * inv_l,
+                                               __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
+                        dst[c * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                p.lse[(size_t)g.bh * p.Sq + row_g] =
+                    (m_used - (F8 ? kF8PShift : 0.f) + lg2_approx(l_run)) * 0.69314718055994531f;
             }
-            fence_proxy_async_smem();
         }
-        named_bar_sync(1 + t, 128);
-        if (my_act && ok && row == 0 && *abort_flag == 0u) {
+        if constexpr (tma_epilogue) {
+            // ---- O / l -> bf16 -> shared memory (this sub-tile's Q buffer) ->
+            // TMA store; LSE.  Both named barriers run whatever `ok` says, so
+            // no warp can be left waiting.
+            named_bar_sync(1 + t, 128);
+            const uint32_t sO = sQ + t * C::QT_BYTES;
+            const int row_g = g.row0 + t * C::BM + row;
+            if (staged && ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l_run;
 #pragma unroll
-            for (int c = 0; c < C::O_NCH; ++c)
-                tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, row0 + t * C::BM, bh);
-            bulk_commit_group();
-            bulk_wait_group_read0();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tm + c * 32, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int U = c * 4 + u;  // 16-byte unit (8 columns) of the row
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv_l,
+                                               __uint_as_float(o[u * 8 + 2 * e + 1]) * inv_l);
+                        const uint32_t addr = sO + (U >> 3) * C::CHUNK + row * 128 +
+                                              ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
+                        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            named_bar_sync(1 + t, 128);
+            if (staged && ok && row == 0 && *abort_flag == 0u) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, g.row0 + t * C::BM, g.bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+            }
+            if (staged && ok && row_g < p.Sq)
+                p.lse[(size_t)g.bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
         }
-        if (my_act && ok && row_g < p.Sq)
-            p.lse[(size_t)bh * p.Sq + row_g] =
-                (m_used - (F8 ? kF8PShift : 0.f) + lg2_approx(l_run)) * 0.69314718055994531f;
     }
 
     tc_fence_before();
@@ -675,31 +835,42 @@ int fwd_smem_bytes(int D) {
     return D == 64 ? (int)FwdCfg<64, false>::SMEM : (int)FwdCfg<128, false>::SMEM;
 }
 
-template <int D, bool WIN, bool F8>
+template <int D, bool WIN, bool F8, bool PERSIST>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas,
-                                cudaStream_t stream) {
+                                const CUtensorMap &tm_o, const FwdParams &p, int n_ctas, cudaStream_t stream) {
     constexpr uint32_t smem = FwdCfg<D, F8>::SMEM;
     cudaError_t e =
-        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fa_fwd_sm103a<D, WIN, F8><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, tm_o, p);
+    fa_fwd_sm103a<D, WIN, F8, PERSIST><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, tm_o, p);
     return cudaGetLastError();
 }
 
+// Persistent CTAs (one per SM, each walking many items) pay off where items
+// differ in length (causal: longest first, dealt out in snake order), where
+// they are short (D = 64) and on the 8-bit path; for long, equal items of
+// 16-bit inputs (full attention, bounded bands) one CTA per item with its
+// TMA-store epilogue measured faster.
+static int grid_for(const FwdParams &p, bool persistent, int num_sms) {
+    return (persistent && p.n_items > num_sms) ? num_sms : p.n_items;
+}
+
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream) {
+                       const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
+    const bool persistent = D == 64 || (!win && p.causal);
+    const int n_ctas = grid_for(p, persistent, num_sms);
     if (D == 64)
-        return win ? launch_fwd_d<64, true, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-                   : launch_fwd_d<64, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    return win ? launch_fwd_d<128, true, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-               : launch_fwd_d<128, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+        return win ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+                   : launch_fwd_d<64, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    if (win) return launch_fwd_d<128, true, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    return persistent ? launch_fwd_d<128, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
+                      : launch_fwd_d<128, false, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream) {
-    return launch_fwd_d<128, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+                           const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream) {
+    return launch_fwd_d<128, false, true, true>(tm_q, tm_k, tm_v, tm_o, p, grid_for(p, true, num_sms), stream);
 }
 
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream) {

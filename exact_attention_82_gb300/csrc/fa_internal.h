@@ -13,9 +13,12 @@ constexpr int kBlockN = 128;  // keys per K/V tile
 
 // Runtime parameters of one forward launch.
 struct FwdParams {
+    void *o;           // [B*H, Sq, D] bf16
     float *lse;        // [B*H, Sq] fp32
     int Sq, Sk;
     int n_mblk;        // ceil(Sq / kCtaRows)
+    int bh_count;      // B * H
+    int n_items;       // n_mblk * B * H work items (256 query rows of one head each)
     int n_kv;          // ceil(Sk / kBlockN)
     int causal;        // longest-first query-block order (triangular work)
     int wl, wr;        // key j allowed for query i iff i-wl <= j <= i+wr; -1 = unbounded
@@ -69,14 +72,15 @@ cudaError_t bwd_status_read_and_clear(int *out);
 // Dynamic shared memory the forward kernel for head dim D asks for.
 int fwd_smem_bytes(int D);
 
-// Launch the forward kernel for head dim D (64 or 128) over n_ctas tiles.
-cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                       const CUtensorMap &tm_v, const CUtensorMap &tm_o, const FwdParams &p,
-                       long long n_ctas, cudaStream_t stream);
+// Launch the forward kernel for head dim D (64 or 128) over the p.n_items
+// work items: persistent CTAs (at most num_sms) or one CTA per item, chosen
+// by the kind of attention; tm_o is the TMA map of O for the latter.
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream);
 
 // Launch the 8-bit (e4m3 Q, K, V; D = 128; full or causal) forward kernel.
 cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_o, const FwdParams &p, long long n_ctas, cudaStream_t stream);
+                           const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream);
 
 // Device status word: read it (after synchronising `stream`) and reset it.
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream);
