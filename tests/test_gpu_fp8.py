@@ -144,3 +144,10 @@ def test_fp8_rejects_bad_arguments():
     z64 = torch.zeros(1, 1, 128, 64, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FAError):
         fa.fa_fwd_fp8(z64, z64, z64, 1.0, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_fp8_parity_many_items(causal):
+    """More items than SMs (persistent CTAs hand buffers over between items),
+    ragged last query block."""
+    parity(2, 100, 300, 300, causal, seed=808 + int(causal))

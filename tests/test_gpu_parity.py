@@ -167,3 +167,30 @@ def test_scores_growing_past_first_tile_max(D, lift, causal):
     og, lg = run_gpu(q, k, v, D ** -0.5, causal)
     ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), D ** -0.5, causal)
     compare(og, lg, *ref, f"lift {lift} D{D}")
+
+
+# ------------------------------------------------- many items per launch
+# More (query block, head) items than SMs, so persistent CTAs walk several
+# items each and hand Q and O buffers over between them; ragged lengths leave
+# the second sub-tile empty in some items.  Every element against the oracle.
+MANY = [
+    # B, H, S, D, causal
+    (2, 80, 300, 128, True),
+    (3, 64, 600, 64, True),
+    (2, 90, 333, 64, False),
+    (1, 160, 257, 128, False),
+]
+
+
+@pytest.mark.parametrize("case", MANY, ids=lambda c: "b{}h{}s{}d{}{}".format(*c[:4], "c" if c[4] else ""))
+def test_parity_many_items(case):
+    B, H, S, D, causal = case
+    full_parity(B, H, S, S, D, causal, seed=4242 + S + H)
+
+
+def test_window_many_items():
+    """D = 64 bounded bands run on persistent CTAs too."""
+    q, k, v = make_qkv(2, 80, 500, 500, 64, seed=77)
+    og, lg = run_gpu(q, k, v, 0.125, False, window=(100, 0))
+    ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), 0.125, False, (100, 0))
+    compare(og, lg, *ref, "window (100, 0), 160 heads")
