@@ -27,6 +27,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -337,7 +339,7 @@ def run_e2e(args, w, q, k, v, dev, world, descales=None):
     import exact_attention_82_gb300 as fa
 
     if w.path == "bwd":
-        return None  # the end-to-end leg times forward outputs; backward runs on device data
+        return run_e2e_bwd(args, w, q, k, v, dev, world)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16).pin_memory()
     hl = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
@@ -379,6 +381,51 @@ def run_e2e(args, w, q, k, v, dev, world, descales=None):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def run_e2e_bwd(args, w, q, k, v, dev, world):
+    """The backward end to end: every step copies Q, K, V, the forward's O and LSE
+    and dO from pinned host memory, runs fa_bwd and reads dQ, dK, dV back."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_82_gb300 as fa
+
+    dq_, dk_, dv_ = (t.to(dev) for t in (q, k, v))
+    fo, flse, dout = make_workspace(fa, w, dq_, dk_, dv_, dev)[:3]
+    host_in = [t.pin_memory() for t in (q, k, v)] + [t.cpu().pin_memory() for t in (fo, flse, dout)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    grads = [torch.empty_like(t) for t in (dq_, dk_, dv_)]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in grads]
+    delta = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        fa.fa_bwd(*dev_in, dq=grads[0], dk=grads[1], dv=grads[2], delta=delta, scale=w.scale,
+                  causal=w.causal, stream=stream)
+        for h, d in zip(host_out, grads):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    return {"value": round(whole_job_tflops(w.flops, world, ms), 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+
+
 # ------------------------------------------------------- CPU (oracle) legs
 def _host_cores():
     try:
@@ -387,9 +434,10 @@ def _host_cores():
         return os.cpu_count() or 1
 
 
-def _oracle_sample(w, qb, kb, vb, heads, descales=None):
+def _oracle_sample(w, qb, kb, vb, heads, descales=None, gb=None):
     """Oracle over the first `heads` (b,h) pairs, all rows; returns (seconds, flops).
-    qb, kb, vb: bf16 bit patterns, or e4m3 codes when `descales` is given."""
+    qb, kb, vb: bf16 bit patterns, or e4m3 codes when `descales` is given; for the
+    backward `gb` holds dO's bf16 bits and the oracle's backward is timed."""
     import oracle
 
     BH = w.B * w.H
@@ -397,12 +445,22 @@ def _oracle_sample(w, qb, kb, vb, heads, descales=None):
     ks = kb.reshape(BH, w.Sk, w.D)[:heads][None]
     vs = vb.reshape(BH, w.Sk, w.D)[:heads][None]
     t0 = time.perf_counter()
-    if descales is not None:
+    if w.path == "bwd":
+        gs = gb.reshape(BH, w.Sq, w.D)[:heads][None]
+        oracle.attn_bwd(qs, ks, vs, gs, w.scale, w.causal, nthreads=_host_cores())
+    elif descales is not None:
         oracle.attn_fwd_fp8(qs, ks, vs, *descales, w.scale, w.causal, nthreads=_host_cores())
     else:
         oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, w.window, nthreads=_host_cores())
     dt = time.perf_counter() - t0
     return dt, w.flops / BH * heads
+
+
+def _dout_bits(w):
+    """dO of the backward workloads (the draw bench.py's own leg uses), as bf16 bits."""
+    from exact_attention_82_gb300.inputs import SEED_BASE, bf16_bits, make_qkv
+
+    return bf16_bits(make_qkv(w.B, w.H, w.Sq, w.Sk, w.D, SEED_BASE + 999)[0])
 
 
 def _oracle_inputs(q, k, v, descales):
@@ -416,42 +474,130 @@ def cpu_baseline(w, q, k, v, target_s, descales=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the
     same workload: whole heads, grown until about `target_s` seconds."""
     qb, kb, vb = _oracle_inputs(q, k, v, descales)
+    gb = _dout_bits(w) if w.path == "bwd" else None
     cores = _host_cores()
     BH = w.B * w.H
     heads = min(BH, cores)
-    dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
+    dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales, gb)
     if dt < target_s / 4 and heads < BH:
         heads = min(BH, max(heads + 1, int(heads * target_s / max(dt, 1e-3) * 0.8)))
-        dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
+        dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales, gb)
+    what = "backward (dQ, dK, dV)" if w.path == "bwd" else "forward"
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": f"{heads} of {BH} (batch,head) pairs of {w.name}, every query row; "
-                      f"fp64 C oracle with S and P materialised"}
+                      f"fp64 C oracle {what} with S and P materialised"}
+
+
+REFERENCE_BUDGET_S = 120.0  # host time of a whole --impl reference run (warm-up + timed steps)
+
+
+class _RowSampler:
+    """Samples of a workload for the reference arm: `rows` consecutive query rows
+    of one head, evaluated by the oracle on exactly the keys those rows may see
+    (the key range and band are re-expressed in the slice's own indices), so a
+    sample's work is exactly that of those rows in the full workload."""
+
+    def __init__(self, w, q, k, v, descales):
+        import oracle
+
+        self.w = w
+        BH = w.B * w.H
+        if descales is not None:
+            conv = [lambda t, d=d: oracle.e4m3_to_f64(t.numpy()) * float(np.float32(d)) for d in descales]
+        else:
+            conv = [lambda t: oracle.bf16_bits_to_f64(t.view(torch_int16()).numpy().view(np.uint16))] * 3
+        self.heads = [t.reshape(BH, -1, w.D) for t in (q, k, v)]
+        self.conv = conv
+        self.g = None
+        if w.path == "bwd":
+            from exact_attention_82_gb300.inputs import SEED_BASE, make_qkv
+
+            self.g = make_qkv(w.B, w.H, w.Sq, w.Sk, w.D, SEED_BASE + 999)[0].reshape(BH, w.Sq, w.D)
+        self.cache = {}
+
+    def _head(self, h):
+        if h not in self.cache:
+            import oracle
+
+            qs, ks, vs = (c(t[h]) for c, t in zip(self.conv, self.heads))
+            gs = None
+            if self.g is not None:
+                gs = oracle.bf16_bits_to_f64(self.g[h].view(torch_int16()).numpy().view(np.uint16))
+            self.cache = {h: (qs, ks, vs, gs)}  # one head at a time
+        return self.cache[h]
+
+    def run(self, h, r0, rows):
+        """Time the oracle on rows r0 .. r0 + rows - 1 of head h; (seconds, flops)."""
+        import oracle
+
+        w = self.w
+        wl, wr = w.window
+        qs, ks, vs, gs = self._head(h)
+        r1 = min(w.Sq, r0 + rows)
+        k0 = max(0, r0 - wl) if wl >= 0 else 0
+        k1 = min(w.Sk, r1 + wr) if wr >= 0 else w.Sk
+        shift = r0 - k0
+        win = (wl - shift if wl >= 0 else -1, wr + shift if wr >= 0 else -1)
+        i = np.arange(r0, r1)
+        lo = np.maximum(0, i - wl) if wl >= 0 else np.zeros_like(i)
+        hi = np.minimum(w.Sk - 1, i + wr) if wr >= 0 else np.full_like(i, w.Sk - 1)
+        pairs = float(np.maximum(hi - lo + 1, 0).sum())
+        flops = 4.0 * w.D * pairs * (2.5 if w.path == "bwd" else 1.0)
+        qa = qs[None, None, r0:r1]
+        ka, va = ks[None, None, k0:k1], vs[None, None, k0:k1]
+        t0 = time.perf_counter()
+        if w.path == "bwd":
+            oracle.attn_bwd(qa, ka, va, gs[None, None, r0:r1], w.scale, False, win, nthreads=_host_cores())
+        else:
+            oracle.attn_fwd(qa, ka, va, w.scale, False, win, nthreads=_host_cores())
+        return time.perf_counter() - t0, flops
+
+
+def torch_int16():
+    import torch
+
+    return torch.int16
 
 
 def run_reference(args):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
-    sample (whole heads) of the same workload."""
+    sample (consecutive query rows of one head, heads and rows advancing from
+    step to step) of the same workload, sized so that the whole run takes about
+    REFERENCE_BUDGET_S seconds whatever --steps and --warmup are."""
     from exact_attention_82_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
     q, k, v, descales = workload_inputs(args.workload)
-    qb, kb, vb = _oracle_inputs(q, k, v, descales)
+    sampler = _RowSampler(w, q, k, v, descales)
     cores = _host_cores()
-    heads = min(w.B * w.H, cores)
-    # size a step to about 3 s of host work, from the first warm-up step
-    dt, _ = _oracle_sample(w, qb, kb, vb, heads, descales)
-    heads = max(1, min(w.B * w.H, int(heads * 3.0 / max(dt, 1e-3))))
-    for _ in range(args.warmup - 1):
-        _oracle_sample(w, qb, kb, vb, heads, descales)
+    per_step = max(0.002, REFERENCE_BUDGET_S / (args.steps + args.warmup))
+    BH = w.B * w.H
+    # calibrate the rows per step on a middle block of head 0
+    rows = min(w.Sq, 32)
+    dt, _ = sampler.run(0, max(0, w.Sq // 2 - rows // 2), rows)
+    rows = max(1, min(w.Sq, int(rows * per_step / max(dt, 1e-6))))
+    pos = [0]
+
+    def step(i):
+        h = i % BH
+        r0 = (pos[0] * rows) % max(1, w.Sq - rows + 1) if rows < w.Sq else 0
+        pos[0] += 1
+        return sampler.run(h, r0, rows)
+
+    for i in range(args.warmup):
+        step(i)
     tot_t, tot_f = 0.0, 0.0
-    for _ in range(args.steps):
-        dt, fl = _oracle_sample(w, qb, kb, vb, heads, descales)
+    for i in range(args.steps):
+        dt, fl = step(args.warmup + i)
         tot_t += dt
         tot_f += fl
     value = tot_f / tot_t / 1e12
-    sample = (f"{heads} of {w.B * w.H} (batch,head) pairs of {w.name} per step, every query "
-              f"row; fp64 C oracle, S and P materialised")
+    what = "backward (dQ, dK, dV)" if w.path == "bwd" else "forward"
+    sample = (f"{rows} consecutive query rows of one (batch, head) of {w.name} per step (of "
+              f"{w.Sq} rows x {BH} heads), heads and rows advancing per step, with exactly the "
+              f"keys they may see; fp64 C oracle {what}, S and P materialised; "
+              f"{REFERENCE_BUDGET_S:.0f} s budget for the whole run")
     return {
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
