@@ -320,6 +320,9 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"independent workload per GPU x{world}",
                    "l2": "flushed before every step (256 MiB write outside the timed events)",
                    "pct_of_bf16_peak": round(100.0 * tflops_launch / peak, 2),
+                   "ms_median": round(statistics.median(times), 5), "ms_min": round(min(times), 5),
+                   "hbm_gbs_algorithmic": round(w.hbm_bytes / (ms_local * 1e-3) / 1e9, 1)
+                   if w.path != "bwd" else None,
                    "wall_s_timed_region": round(t_wall, 4)},
         "roofline": roofline,
         "cpu_baseline": cpu,
