@@ -63,7 +63,9 @@ namespace fa {
 
 __device__ int g_status_word = 0;
 
-template <int D, bool F8>
+// QB: query buffers per sub-tile (2: a persistent CTA loads the next item's Q
+// while the current item runs, where shared memory has room for it).
+template <int D, bool F8, int QB = 1>
 struct FwdCfg {
     static constexpr int BM = kBlockM;  // rows per sub-tile (TMEM lanes)
     static constexpr int BN = kBlockN;  // keys per K/V tile
@@ -75,8 +77,8 @@ struct FwdCfg {
     static constexpr uint32_t QT_BYTES = BM * D * EB;     // one query sub-tile
     static constexpr uint32_t KV_BYTES = BN * D * EB;     // one K or V tile
     static constexpr uint32_t CHUNK = 128 * 128;          // 128 rows x 128 bytes
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
+    static constexpr uint32_t OFF_Q = 0;                  // [QB][sub-tile] query tiles
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * QB * QT_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
     static constexpr uint32_t BAR_BYTES = 384;
@@ -107,17 +109,17 @@ constexpr float kF8Lazy = 2.f;
 
 // barrier slots (8 bytes each) inside the OFF_BAR block
 enum : uint32_t {
-    B_Q_FULL = 0,    // + sub-tile: Q_t of the current item loaded
-    B_Q_FREE = 2,    // + sub-tile: the item's last S_t has read Q_t
-    B_K_FULL = 4,    // + stage (up to 4)
-    B_K_EMPTY = 8,   // + stage
-    B_V_FULL = 12,   // + stage
-    B_V_EMPTY = 16,  // + stage
-    B_S_FULL = 20,   // + sub-tile
-    B_P_FULL = 22,   // + sub-tile
-    B_O_DONE = 24,   // + sub-tile: the item's last P_t V is complete
-    B_O_FREE = 26,   // + sub-tile: the softmax warps have read O_t out (128 arrivals)
-    B_DRAIN = 28,
+    B_Q_FULL = 0,    // + 2 * buffer + sub-tile: an item's Q_t loaded
+    B_Q_FREE = 4,    // + 2 * buffer + sub-tile: that item's last S_t has read Q_t
+    B_K_FULL = 8,    // + stage (up to 4)
+    B_K_EMPTY = 12,  // + stage
+    B_V_FULL = 16,   // + stage
+    B_V_EMPTY = 20,  // + stage
+    B_S_FULL = 24,   // + sub-tile
+    B_P_FULL = 26,   // + sub-tile
+    B_O_DONE = 28,   // + sub-tile: the item's last P_t V is complete
+    B_O_FREE = 30,   // + sub-tile: the softmax warps have read O_t out (128 arrivals)
+    B_DRAIN = 32,
 };
 constexpr uint32_t SLOT_TMEM = 320;   // byte offset of the TMEM base address
 constexpr uint32_t SLOT_ABORT = 324;  // byte offset of the abort flag
@@ -129,6 +131,13 @@ constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+
 // sides then compile without spills (the MMA thread's loop is the critical path).
 constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
+
+// Query buffers per sub-tile: two where they fit in shared memory (D = 64 and
+// the 8-bit path), so that a persistent CTA loads the next item's Q while the
+// current item runs; the 16-bit D = 128 rings leave room for one.
+__host__ __device__ constexpr int query_buffers(int D, bool F8, bool PERSIST) {
+    return (PERSIST && (D == 64 || F8)) ? 2 : 1;
+}
 
 // One work item: 256 query rows (two sub-tiles) of one (batch, head), and the
 // key tiles [jlo_t, jhi_t] each sub-tile needs.  Key tiles are loaded from J
@@ -192,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-    using C = FwdCfg<D, F8>;
+    constexpr int QB = query_buffers(D, F8, PERSIST);
+    using C = FwdCfg<D, F8, QB>;
     static_assert(!(F8 && WIN), "the 8-bit path has no bounded band");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -219,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(B_Q_FULL + i), 1);
+            mbar_init(bar(B_Q_FREE + i), 1);
+        }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(B_Q_FULL + t), 1);
-            mbar_init(bar(B_Q_FREE + t), 1);
             mbar_init(bar(B_S_FULL + t), 1);
             mbar_init(bar(B_P_FULL + t), 128);
             mbar_init(bar(B_O_DONE + t), 1);
@@ -281,13 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
                 const Item g = item_at<WIN>(p, k);
-                // Q_t of this item, once the previous item's last S_t has read the buffer
+                // Q_t of this item into buffer qn % QB, once the last S_t of the item
+                // that used the buffer before has read it
                 auto load_q = [&](int t, int &qn) -> bool {
-                    if (qn > 0 && !wait(B_Q_FREE + t, (uint32_t)(qn - 1) & 1u)) return false;
-                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), C::QT_BYTES);
+                    const int b = qn % QB, use = qn / QB;  // use-th load into buffer b
+                    const uint32_t qb = 2 * b + t;
+                    if (use > 0 && !wait(B_Q_FREE + qb, (uint32_t)(use - 1) & 1u)) return false;
+                    mbar_arrive_expect_tx(bar(B_Q_FULL + qb), C::QT_BYTES);
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(sQ + t * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS, g.row0 + t * C::BM,
-                                    g.bh, bar(B_Q_FULL + t), pol_q);
+                        tma_load_3d(sQ + qb * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS,
+                                    g.row0 + t * C::BM, g.bh, bar(B_Q_FULL + qb), pol_q);
                     ++qn;
                     return true;
                 };
@@ -299,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // wind down: every copy issued here has landed before the CTA may exit
-            if (qn0 > 0) mbar_wait_drain(bar(B_Q_FULL + 0), (uint32_t)(qn0 - 1) & 1u, kDrainNs);
-            if (qn1 > 0) mbar_wait_drain(bar(B_Q_FULL + 1), (uint32_t)(qn1 - 1) & 1u, kDrainNs);
+            for (int i = (qn0 > QB ? qn0 - QB : 0); i < qn0; ++i)
+                mbar_wait_drain(bar(B_Q_FULL + 2 * (i % QB)), (uint32_t)(i / QB) & 1u, kDrainNs);
+            for (int i = (qn1 > QB ? qn1 - QB : 0); i < qn1; ++i)
+                mbar_wait_drain(bar(B_Q_FULL + 2 * (i % QB) + 1), (uint32_t)(i / QB) & 1u, kDrainNs);
             for (int i = (nk > C::KST ? nk - C::KST : 0); i < nk; ++i)
                 mbar_wait_drain(bar(B_K_FULL + i % C::KST), (uint32_t)(i / C::KST) & 1u, kDrainNs);
             for (int i = (nv > C::VST ? nv - C::VST : 0); i < nv; ++i)
@@ -317,8 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // cannot carry: shared addresses < 256 KB), ring stages and phases
             // advance incrementally, and participation is a precomputed
             // iteration range per sub-tile.
-            const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
-            const uint64_t dq1 = sw128_desc(sQ + C::QT_BYTES, 16, 1024);
+            const uint64_t dqb = sw128_desc(sQ, 16, 1024);  // query buffer 0 of sub-tile 0
             const uint64_t dk = sw128_desc(sK, 16, 1024);
             const uint64_t dv = sw128_desc(sV, C::CHUNK, 1024);
             int sk = 0, sv = 0;       // ring stage of the next K and V tile to be read, over all items
@@ -353,7 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             // before an item's first S_t: its Q_t has landed
-            auto q_ready = [&](int t) { return wait(B_Q_FULL + t, (uint32_t)(t ? qn1 : qn0) & 1u); };
+            auto q_ready = [&](int t) {
+                const int q = t ? qn1 : qn0;  // the item's Q_t is the q-th load: buffer q % QB
+                return wait(B_Q_FULL + 2 * (q % QB) + t, (uint32_t)(q / QB) & 1u);
+            };
             // before an item's first P_t V: the softmax warps have read the previous item's O_t
             auto o_free = [&](int t) {
                 const int q = t ? qn1 : qn0;
@@ -363,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item g = item_at<WIN>(p, k);
                 const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
                 const int N = g.N;
+                // this item's query buffers, their descriptors and release barriers
+                const int qb0 = 2 * (qn0 % QB), qb1 = 2 * (qn1 % QB) + 1;
+                const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
+                const uint32_t qf0 = B_Q_FREE + qb0, qf1 = B_Q_FREE + qb1;
                 int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
                 if constexpr (!F8) {
                     // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
@@ -398,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             issue_s(dq0, tmem, sk);
                             tc_commit(bar(B_S_FULL + 0));
                             if constexpr (PERSIST) {
-                                if (it == last0) tc_commit(bar(B_Q_FREE + 0));
+                                if (it == last0) tc_commit(bar(qf0));
                             }
                         }
                         if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
@@ -418,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             issue_s(dq1, tmem + 128, sk);
                             tc_commit(bar(B_S_FULL + 1));
                             if constexpr (PERSIST) {
-                                if (it == last1) tc_commit(bar(B_Q_FREE + 1));
+                                if (it == last1) tc_commit(bar(qf1));
                             }
                         }
                         tc_commit(bar(B_K_EMPTY + sk));
@@ -478,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (s0) {
                             tc_commit(bar(B_S_FULL + 0));
-                            if (it == last0) tc_commit(bar(B_Q_FREE + 0));
+                            if (it == last0) tc_commit(bar(qf0));
                         }
                         // ---- burst B: PV1_{it-1}, S1_it
                         if (pv1) {
@@ -501,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (s1) {
                             tc_commit(bar(B_S_FULL + 1));
-                            if (it == last1) tc_commit(bar(B_Q_FREE + 1));
+                            if (it == last1) tc_commit(bar(qf1));
                         }
                         if (s0 || s1) tc_commit(bar(B_K_EMPTY + sk));
                         if (it < N) {
@@ -831,14 +854,10 @@ __global__ void fa_wait_selftest(unsigned long long limit_ns) {
     __syncthreads();
 }
 
-int fwd_smem_bytes(int D) {
-    return D == 64 ? (int)FwdCfg<64, false>::SMEM : (int)FwdCfg<128, false>::SMEM;
-}
-
 template <int D, bool WIN, bool F8, bool PERSIST>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const CUtensorMap &tm_o, const FwdParams &p, int n_ctas, cudaStream_t stream) {
-    constexpr uint32_t smem = FwdCfg<D, F8>::SMEM;
+    constexpr uint32_t smem = FwdCfg<D, F8, query_buffers(D, F8, PERSIST)>::SMEM;
     cudaError_t e =
         cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
