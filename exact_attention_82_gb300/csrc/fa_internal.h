@@ -69,7 +69,6 @@ cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, cons
                        const BwdParams &p, long long BH, cudaStream_t stream);
 cudaError_t bwd_status_read_and_clear(int *out);
 
-
 // Launch the forward kernel for head dim D (64 or 128) over the p.n_items
 // work items: persistent CTAs (at most num_sms) or one CTA per item, chosen
 // by the kind of attention; tm_o is the TMA map of O for the latter.
