@@ -45,7 +45,7 @@ struct BwdCfg {
     static constexpr uint32_t OFF_B = TILE;            // resident tile 2 (dO or V)
     static constexpr uint32_t OFF_R1 = 2 * TILE;       // ring 1 (K or Q), 2 stages
     static constexpr uint32_t OFF_R2 = 4 * TILE;       // ring 2 (V or dO), 2 stages
-    static constexpr uint32_t OFF_VEC = 6 * TILE;      // [2 parity][2: lse2, delta][128] fp32
+    static constexpr uint32_t OFF_VEC = 6 * TILE;      // [2 parity][2: -lse2, -delta][128] fp32
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * T * 4;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;  // S, dP, accumulator(s)
@@ -212,7 +212,11 @@ __global__ void __launch_bounds__(192, 1)
             p.delta[r] = delta;
             lse2 = p.lse[r] * 1.4426950408889634f;
         }
-        const float sl2 = p.scale_log2;
+        // Packed pairs: p = 2^(s*scale*log2e - lse) and dS = p (dP - Delta) two
+        // columns per instruction.  A row past Sq has lse = +inf, so its p is 0.
+        const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t nl2 = f2_pack(-lse2, -lse2);
+        const uint64_t nd2 = f2_pack(-delta, -delta);
         bool ok = true;
         for (int it = 0; it < N; ++it) {
             if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
@@ -220,33 +224,43 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) break;
             tc_fence_after();
             const int col0 = (j_hi - it) * C::T;
-            const bool masked = it == 0 && mask_first;
             const int lim = (p.causal ? min(p.Sk, row_g + 1) : p.Sk) - col0;
+            // keys at or past `lim` are out (only the first tile: causal diagonal, ragged end)
+            auto chunks = [&](bool masked) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-                uint32_t s[32], dp[32];
-                tmem_ld32(x_tm + c * 32, s);
-                tmem_ld32(y_tm + c * 32, dp);
-                tmem_ld_wait(s);
-                tmem_ld_wait(dp);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+                    uint32_t s[32], dp[32];
+                    tmem_ld32(x_tm + c * 32, s);
+                    tmem_ld32(y_tm + c * 32, dp);
+                    tmem_ld_wait(s);
+                    tmem_ld_wait(dp);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pr[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int cc = c * 32 + 2 * e + h;
-                        float pv = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), sl2, -lse2));
-                        if (!valid_row || (masked && cc >= lim)) pv = 0.f;
-                        pr[h] = pv * (__uint_as_float(dp[2 * e + h]) - delta);
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), c2, nl2),
+                                  x0, x1);
+                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        if (masked) {
+                            if (c * 32 + 2 * e >= lim) p0 = 0.f;
+                            if (c * 32 + 2 * e + 1 >= lim) p1 = 0.f;
+                        }
+                        float d0, d1;
+                        f2_unpack(f2_mul(f2_pack(p0, p1),
+                                         f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), nd2)),
+                                  d0, d1);
+                        pk[e] = b16_pack(d0, d1);
                     }
-                    pk[e] = b16_pack(pr[0], pr[1]);
+                    tmem_st16(x_tm + c * 16, pk);
+                    tmem_st_wait16(pk);
+                    tc_fence_before();
+                    mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
                 }
-                tmem_st16(x_tm + c * 16, pk);
-                tmem_st_wait16(pk);
-                tc_fence_before();
-                mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
-            }
+            };
+            if (it == 0 && mask_first)
+                chunks(true);
+            else
+                chunks(false);
         }
         // ---- epilogue: dQ = scale * acc -> bf16 -> shared (the Q tile) -> TMA store
         if (ok) ok = wait(BB_DONE, 0);
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(192, 1)
     auto bar = [&](uint32_t i) { return bars + 8u * i; };
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_ABORT);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_TMEM);
-    float *vec = reinterpret_cast<float *>(gbase + C::OFF_VEC);  // [parity][lse2 | delta][128]
+    float *vec = reinterpret_cast<float *>(gbase + C::OFF_VEC);  // [parity][-lse2 | -delta][128]
     if (threadIdx.x == 0) {
         mbar_init(bar(BB_RES), 1);
         for (int s = 0; s < 2; ++s) {
@@ -416,53 +430,69 @@ __global__ void __launch_bounds__(192, 1)
         const int key_g = nt * C::T + row;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t x_tm = tmem + lane_off + C::TM_X, y_tm = tmem + lane_off + C::TM_Y;
-        const float sl2 = p.scale_log2;
+        const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int it = 0; it < N; ++it) {
-            // this tile's query rows: lse (exp2 units; +inf past Sq, so P = 0) and Delta
+            // this tile's query rows, negated for the packed arithmetic below: -lse
+            // (exp2 units; -inf past Sq, so P = 0) and -Delta
             const int qt = i_lo + it;
             float *lv = vec + (it & 1) * 256;
             {
                 const int qg = qt * C::T + row;
                 const size_t r = (size_t)bh * p.Sq + qg;
-                lv[row] = qg < p.Sq ? p.lse[r] * 1.4426950408889634f : INFINITY;
-                lv[128 + row] = qg < p.Sq ? p.delta[r] : 0.f;
+                lv[row] = qg < p.Sq ? -(p.lse[r] * 1.4426950408889634f) : -INFINITY;
+                lv[128 + row] = qg < p.Sq ? -p.delta[r] : 0.f;
             }
             named_bar_sync(1, 128);
             if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                const bool masked = it == 0 && mask_first;  // diagonal: keys above the query are out
+                // columns (queries) in pairs: (-lse, -Delta) of queries cc, cc+1 as
+                // one 64-bit shared load each; P^T and dS^T two columns per instruction
+                const uint64_t *nl = reinterpret_cast<const uint64_t *>(lv);
+                const uint64_t *nd = reinterpret_cast<const uint64_t *>(lv + 128);
+                const int lim = key_g - qt * C::T;  // diagonal tile: query cc sees this key iff cc >= lim
+                auto chunks = [&](bool masked) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16], dk[16];
-                    uint32_t s[32], dp[32];
-                    tmem_ld32(x_tm + c * 32, s);
-                    tmem_ld32(y_tm + c * 32, dp);
-                    tmem_ld_wait(s);
-                    tmem_ld_wait(dp);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16], dk[16];
+                        uint32_t s[32], dp[32];
+                        tmem_ld32(x_tm + c * 32, s);
+                        tmem_ld32(y_tm + c * 32, dp);
+                        tmem_ld_wait(s);
+                        tmem_ld_wait(dp);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float pr[2], ds[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int cc = c * 32 + 2 * e + h;  // query within the tile
-                            float pv = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), sl2, -lv[cc]));
-                            if (masked && key_g > qt * C::T + cc) pv = 0.f;
-                            pr[h] = pv;
-                            ds[h] = pv * (__uint_as_float(dp[2 * e + h]) - lv[128 + cc]);
+                        for (int e = 0; e < 16; ++e) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), c2,
+                                             nl[c * 16 + e]),
+                                      x0, x1);
+                            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            if (masked) {
+                                if (c * 32 + 2 * e < lim) p0 = 0.f;
+                                if (c * 32 + 2 * e + 1 < lim) p1 = 0.f;
+                            }
+                            float d0, d1;
+                            f2_unpack(f2_mul(f2_pack(p0, p1),
+                                             f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                                    nd[c * 16 + e])),
+                                      d0, d1);
+                            pk[e] = b16_pack(p0, p1);
+                            dk[e] = b16_pack(d0, d1);
                         }
-                        pk[e] = b16_pack(pr[0], pr[1]);
-                        dk[e] = b16_pack(ds[0], ds[1]);
+                        tmem_st16(x_tm + c * 16, pk);
+                        tmem_st16(y_tm + c * 16, dk);
+                        tmem_st_wait16(pk);
+                        tmem_st_wait16(dk);
+                        tc_fence_before();
+                        mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
                     }
-                    tmem_st16(x_tm + c * 16, pk);
-                    tmem_st16(y_tm + c * 16, dk);
-                    tmem_st_wait16(pk);
-                    tmem_st_wait16(dk);
-                    tc_fence_before();
-                    mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
-                }
+                };
+                if (it == 0 && mask_first)  // diagonal: keys above the query are out
+                    chunks(true);
+                else
+                    chunks(false);
             }
         }
         // ---- epilogue: dV and scale * dK -> bf16 -> shared (the K and V tiles) -> TMA store
