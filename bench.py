@@ -333,100 +333,116 @@ def run_ours(args, rank, world, local_rank):
     }
 
 
-def run_e2e(args, w, q, k, v, dev, world, descales=None):
-    """Same metric through the public call with host buffers: every step copies
-    Q, K, V from pinned host memory, runs fa_fwd and reads O and LSE back."""
+def _pipelined_e2e(args, host_in, host_out, launch, dev, world, flops):
+    """End-to-end steps through the public call: step i copies `host_in` (pinned)
+    to the device, calls `launch(dev_in, dev_out, stream)` and reads `dev_out`
+    back into `host_out` (pinned).  Steps are pipelined as a serving loop runs
+    them, with two sets of device buffers: the input copy of step i+1 (its own
+    stream) overlaps step i's call, and step i's read-back (a third stream)
+    overlaps step i+1.  Every step's copies lie inside the timed region, which
+    starts before the first input copy and ends after the last read-back."""
     import torch
     import torch.distributed as dist
+
+    dev_in = [[torch.empty_like(h, device=dev) for h in host_in] for _ in range(2)]
+    dev_out = [[torch.empty_like(h, device=dev) for h in host_out] for _ in range(2)]
+    compute = torch.cuda.current_stream(dev)
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(steps):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(compute)
+        h2d.wait_stream(compute)
+        ready, used, read = [None, None], [None, None], [None, None]
+
+        def load(i):
+            b = i & 1
+            if used[b] is not None:  # step i-2's call is done with these inputs
+                h2d.wait_event(used[b])
+            with torch.cuda.stream(h2d):
+                for d, h in zip(dev_in[b], host_in):
+                    d.copy_(h, non_blocking=True)
+            ready[b] = torch.cuda.Event()
+            ready[b].record(h2d)
+
+        load(0)
+        for i in range(steps):
+            b = i & 1
+            if i + 1 < steps:
+                load(i + 1)
+            compute.wait_event(ready[b])
+            if read[b] is not None:  # step i-2's outputs have been read back
+                compute.wait_event(read[b])
+            launch(dev_in[b], dev_out[b], compute)
+            used[b] = torch.cuda.Event()
+            used[b].record(compute)
+            d2h.wait_event(used[b])
+            with torch.cuda.stream(d2h):
+                for h, d in zip(host_out, dev_out[b]):
+                    h.copy_(d, non_blocking=True)
+            read[b] = torch.cuda.Event()
+            read[b].record(d2h)
+        compute.wait_stream(h2d)
+        compute.wait_stream(d2h)
+        end.record(compute)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    run(3)
+    if world > 1:
+        dist.barrier()
+    steps = max(3, min(args.steps, 50))
+    ms = max_over_ranks(run(steps) / steps, world, dev)
+    return {"value": round(whole_job_tflops(flops, world, ms), 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out),
+            "overlap": "step i+1's input copy and step i's read-back run beside step i's call "
+                       "(three streams, two device buffer sets)"}
+
+
+def run_e2e(args, w, q, k, v, dev, world, descales=None):
+    """Same metric through the public call with host buffers: every step copies
+    Q, K, V from pinned host memory, runs the attention call and reads O and LSE
+    back (pipelined across steps, see _pipelined_e2e)."""
+    import torch
 
     import exact_attention_82_gb300 as fa
 
     if w.path == "bwd":
         return run_e2e_bwd(args, w, q, k, v, dev, world)
-    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-    ho = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
-    dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
-    do = torch.empty_like(ho, device=dev)
-    dl = torch.empty_like(hl, device=dev)
-    dq.copy_(hq)
-    dk.copy_(hk)
-    dv.copy_(hv)
-    ws = make_workspace(fa, w, dq, dk, dv, dev, descales)
-    stream = torch.cuda.current_stream()
-    steps = max(3, min(args.steps, 50))
+    host_in = [t.pin_memory() for t in (q, k, v)]
+    host_out = [torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()]
+    ws = make_workspace(fa, w, *host_in, dev, descales)  # (Q, K, V only matter on the backward path)
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        run_path(fa, w, dq, dk, dv, do, dl, ws, stream)
-        ho.copy_(do, non_blocking=True)
-        hl.copy_(dl, non_blocking=True)
+    def launch(din, dout, stream):
+        run_path(fa, w, *din, *dout, ws, stream)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-    return {"value": round(whole_job_tflops(w.flops, world, ms), 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    return _pipelined_e2e(args, host_in, host_out, launch, dev, world, w.flops)
 
 
 def run_e2e_bwd(args, w, q, k, v, dev, world):
     """The backward end to end: every step copies Q, K, V, the forward's O and LSE
-    and dO from pinned host memory, runs fa_bwd and reads dQ, dK, dV back."""
+    and dO from pinned host memory, runs fa_bwd and reads dQ, dK, dV back
+    (pipelined across steps, see _pipelined_e2e)."""
     import torch
-    import torch.distributed as dist
 
     import exact_attention_82_gb300 as fa
 
     dq_, dk_, dv_ = (t.to(dev) for t in (q, k, v))
     fo, flse, dout = make_workspace(fa, w, dq_, dk_, dv_, dev)[:3]
     host_in = [t.pin_memory() for t in (q, k, v)] + [t.cpu().pin_memory() for t in (fo, flse, dout)]
-    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
-    grads = [torch.empty_like(t) for t in (dq_, dk_, dv_)]
-    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in grads]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq_, dk_, dv_)]
     delta = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-    steps = max(3, min(args.steps, 50))
+    del dq_, dk_, dv_, fo, flse, dout
 
-    def step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        fa.fa_bwd(*dev_in, dq=grads[0], dk=grads[1], dv=grads[2], delta=delta, scale=w.scale,
+    def launch(din, dout, stream):
+        fa.fa_bwd(*din, dq=dout[0], dk=dout[1], dv=dout[2], delta=delta, scale=w.scale,
                   causal=w.causal, stream=stream)
-        for h, d in zip(host_out, grads):
-            h.copy_(d, non_blocking=True)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
-    return {"value": round(whole_job_tflops(w.flops, world, ms), 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+    return _pipelined_e2e(args, host_in, host_out, launch, dev, world, w.flops)
 
 
 # ------------------------------------------------------- CPU (oracle) legs
