@@ -20,7 +20,8 @@
 //                feed dV += P^T dO and dK += dS^T Q.
 // P is recomputed from the saved LSE, as the forward's epilogue stores it.
 // Both kernels: warps 0-3 element-wise (thread = TMEM lane = output row),
-// warp 4 TMA producer, warp 5 TMEM allocation and single-thread MMA issue.
+// warp 4 TMA producer, warp 5 TMEM allocation and MMA issue (the whole warp
+// runs the issue loop, one elected lane issues each instruction).
 // Rows are handled in 32-column chunks; chunk c's bf16 result is written to
 // columns [16c, 16c+16), all of which the thread has already read.
 #include <math.h>
@@ -143,7 +144,11 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_wait_drain(bar(BB_FULL + (it & 1)), (uint32_t)(it >> 1) & 1u, kBwdDrainNs);
         }
     } else if (warp == 5) {
-        if (lane == 0) {  // ---- MMA issue
+        {  // ---- MMA issue: the whole warp runs the loop, one elected lane issues
+            auto wait = [&](uint32_t b, uint32_t parity) {
+                return __all_sync(0xffffffffu,
+                                  mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT));
+            };
             const uint64_t da = sw128_desc(sbase + C::OFF_A, 16, 1024);   // Q, K-major
             const uint64_t db = sw128_desc(sbase + C::OFF_B, 16, 1024);   // dO, K-major
             const uint64_t dk1 = sw128_desc(sbase + C::OFF_R1, 16, 1024);         // K as B of S (K-major)
@@ -381,7 +386,11 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_wait_drain(bar(BB_FULL + (it & 1)), (uint32_t)(it >> 1) & 1u, kBwdDrainNs);
         }
     } else if (warp == 5) {
-        if (lane == 0) {  // ---- MMA issue
+        {  // ---- MMA issue: the whole warp runs the loop, one elected lane issues
+            auto wait = [&](uint32_t b, uint32_t parity) {
+                return __all_sync(0xffffffffu,
+                                  mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT));
+            };
             const uint64_t dka = sw128_desc(sbase + C::OFF_A, 16, 1024);          // K, K-major (A of S^T)
             const uint64_t dva = sw128_desc(sbase + C::OFF_B, 16, 1024);          // V, K-major (A of dP^T)
             const uint64_t dq1 = sw128_desc(sbase + C::OFF_R1, 16, 1024);         // Q as B of S^T
