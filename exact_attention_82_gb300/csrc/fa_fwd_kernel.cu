@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
                 const uint32_t qf0 = B_Q_FREE + qb0, qf1 = B_Q_FREE + qb1;
                 int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
-                if constexpr (!F8) {
+                {
                     // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
                     int svp = 0;          // V stage of the previous tile
                     uint32_t vpph = 0;
@@ -471,77 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok) {
                             tc_commit(bar(B_O_DONE + 1));
                             tc_commit(bar(B_V_EMPTY + svp));
-                        }
-                    }
-                } else {
-                    // The same MMA order, grouped into two bursts per step:
-                    // [PV0_{j-1}, S0_j] and [PV1_{j-1}, S1_j].  Every wait a burst
-                    // needs is taken before it and every commit after it, so each
-                    // step has two gaps in the MMA stream instead of four; that
-                    // pays where MMAs are short (8-bit: half the tensor time per
-                    // instruction), while the 16-bit kernel is faster with the
-                    // loop above.  Step j = N issues only the last P V.
-                    for (int it = 0; ok && it <= N; ++it) {
-                        const bool pv0 = it - 1 >= first0 && it - 1 <= last0;  // PV0 of tile it-1
-                        const bool s0 = it < N && it >= first0 && it <= last0;
-                        const bool pv1 = it - 1 >= first1 && it - 1 <= last1;
-                        const bool s1 = it < N && it >= first1 && it <= last1;
-                        // ---- burst A: PV0_{it-1}, S0_it
-                        if (pv0) {
-                            ok = wait(B_P_FULL + 0, (uint32_t)npv0 & 1u) && wait(B_V_FULL + sv, vph) &&
-                                 (ipv0 > 0 || o_free(0));
-                            if (!ok) break;
-                        }
-                        if (s0 || s1) {
-                            ok = wait(B_K_FULL + sk, kph);
-                            if (!ok) break;
-                        }
-                        if (s0 && it == first0) {
-                            ok = q_ready(0);
-                            if (!ok) break;
-                        }
-                        tc_fence_after();
-                        if (pv0) issue_pv_mma(0, ipv0 > 0, sv);
-                        if (s0) issue_s(dq0, tmem, sk);
-                        if (pv0) {
-                            if (it - 1 == last0) tc_commit(bar(B_O_DONE + 0));
-                            if (!pv1) tc_commit(bar(B_V_EMPTY + sv));
-                            ++npv0;
-                            ++ipv0;
-                        }
-                        if (s0) {
-                            tc_commit(bar(B_S_FULL + 0));
-                            if (it == last0) tc_commit(bar(qf0));
-                        }
-                        // ---- burst B: PV1_{it-1}, S1_it
-                        if (pv1) {
-                            ok = wait(B_P_FULL + 1, (uint32_t)npv1 & 1u) && (pv0 || wait(B_V_FULL + sv, vph)) &&
-                                 (ipv1 > 0 || o_free(1));
-                            if (!ok) break;
-                        }
-                        if (s1 && it == first1) {
-                            ok = q_ready(1);
-                            if (!ok) break;
-                        }
-                        if (pv1 || (s1 && it == first1)) tc_fence_after();
-                        if (pv1) issue_pv_mma(1, ipv1 > 0, sv);
-                        if (s1) issue_s(dq1, tmem + 128, sk);
-                        if (pv1) {
-                            if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
-                            tc_commit(bar(B_V_EMPTY + sv));
-                            ++npv1;
-                            ++ipv1;
-                        }
-                        if (s1) {
-                            tc_commit(bar(B_S_FULL + 1));
-                            if (it == last1) tc_commit(bar(qf1));
-                        }
-                        if (s0 || s1) tc_commit(bar(B_K_EMPTY + sk));
-                        if (it < N) {
-                            if (++sk == C::KST) { sk = 0; kph ^= 1u; }
-                        }
-                        if (it >= 1) {
-                            if (++sv == C::VST) { sv = 0; vph ^= 1u; }
                         }
                     }
                 }
@@ -875,11 +804,11 @@ static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k
     return cudaGetLastError();
 }
 
-// Persistent CTAs (one per SM, each walking many items) pay off where items
-// differ in length (causal: longest first, dealt out in snake order), where
-// they are short (D = 64) and on the 8-bit path; for long, equal items of
-// 16-bit inputs (full attention, bounded bands) one CTA per item with its
-// TMA-store epilogue measured faster.
+// Persistent CTAs (one per SM, each walking many items) take the fixed cost
+// of a CTA off every item but the first and even out items of different
+// length (causal: longest first, dealt out in snake order); for the bounded
+// bands of D = 128, one CTA per item with its TMA-store epilogue measured
+// faster.
 static int grid_for(const FwdParams &p, bool persistent, int num_sms) {
     return (persistent && p.n_items > num_sms) ? num_sms : p.n_items;
 }
@@ -887,14 +816,13 @@ static int grid_for(const FwdParams &p, bool persistent, int num_sms) {
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
-    const bool persistent = D == 64 || (!win && p.causal);
+    const bool persistent = D == 64 || !win;
     const int n_ctas = grid_for(p, persistent, num_sms);
     if (D == 64)
         return win ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
                    : launch_fwd_d<64, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
     if (win) return launch_fwd_d<128, true, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    return persistent ? launch_fwd_d<128, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-                      : launch_fwd_d<128, false, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+    return launch_fwd_d<128, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
