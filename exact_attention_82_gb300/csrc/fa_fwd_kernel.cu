@@ -8,9 +8,10 @@
 //
 // Mapping onto the chip.  The work items are the (query block, batch x head)
 // pairs of the same page's launch grid (section "第一处源码差异：launch grid
-// 怎么铺"); the kernel is persistent: one CTA per SM takes one item per round
-// of gridDim.x items, in snake order (causal: all heads' longest query
-// blocks first).  TMEM is allocated and the barriers initialised once, and the next
+// 怎么铺"); for full and causal attention the kernel is persistent: one CTA
+// per SM takes one item per round of gridDim.x items, in snake order (causal:
+// all heads' longest query blocks first; a bounded band runs one CTA per
+// item).  TMEM is allocated and the barriers initialised once, and the next
 // item's Q and first K/V tiles load while the current item finishes, which
 // takes the fixed cost of a CTA (launch, setup, load latency, epilogue) off
 // every item but the first.  Each item is 256 query rows as two 128-row
@@ -129,7 +130,7 @@ constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+
 // Register split.  At launch every thread has 168 (3 warps per SM sub-partition);
 // the MMA/TMA warpgroup drops to 104 and the softmax warpgroups rise to 200:
 // 256 x 200 + 128 x 104 = 64512 = 384 x 168, the block's launch total.  Both
-// sides then compile without spills (the MMA thread's loop is the critical path).
+// sides then compile without spills (the MMA-issue loop is the critical path).
 constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
 
@@ -196,7 +197,7 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
 // F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
 // PERSIST: the grid may be smaller than the item count, so a CTA walks items
 // and hands Q and O buffers over between them; without it every CTA has one
-// item and the hand-over code is compiled out of the MMA thread's loop.
+// item and the hand-over code is compiled out of the MMA-issue loop.
 template <int D, bool WIN, bool F8, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -492,10 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         int ns = 0;  // S_t tiles so far, over all items (S_FULL phases)
         int od = 0;  // items so far in which this sub-tile took part (O_DONE phases)
-        // With one item per CTA (not PERSIST) and 16-bit inputs, O is staged in this sub-tile's Q buffer, free once the
-        // item's MMAs are done, and written by a TMA store after the loop;
-        // a persistent CTA stores each row directly, so that its Q buffer
-        // can take the next item's Q as early as possible.
+        // With one item per CTA (not PERSIST) and 16-bit inputs, O is staged in
+        // this sub-tile's Q buffer, free once the item's MMAs are done, and
+        // written by a TMA store after the loop; a persistent CTA stores each
+        // row directly, so that its Q buffer can take the next item's Q as
+        // early as possible.
         constexpr bool tma_epilogue = !F8 && !PERSIST;
         bool ok = true, staged = false;
         Item g;
