@@ -65,22 +65,26 @@ namespace fa {
 
 __device__ int g_status_word = 0;
 
-// QB: query buffers per sub-tile (2: a persistent CTA loads the next item's Q
-// while the current item runs, where shared memory has room for it).
+// QB: query buffers per sub-tile, 1 or 2 (2: a persistent CTA loads the next
+// item's Q while the current item runs, where shared memory has room for it);
+// or QB = 3: a ring of three query tiles shared by the two sub-tiles, one K
+// stage fewer, so that a persistent CTA loads the next item's Q_0 a whole item
+// ahead (16-bit inputs, D = 128).
 template <int D, bool F8, int QB = 1>
 struct FwdCfg {
     static constexpr int BM = kBlockM;  // rows per sub-tile (TMEM lanes)
     static constexpr int BN = kBlockN;  // keys per K/V tile
     static constexpr int EB = F8 ? 1 : 2;                 // bytes per Q/K/V element
-    static constexpr int KST = (F8 || D == 64) ? 4 : 3;
+    static constexpr int NQ = QB == 3 ? 3 : 2 * QB;       // query tile slots
+    static constexpr int KST = (F8 || D == 64) ? 4 : (QB == 3 ? 2 : 3);
     static constexpr int VST = (F8 || D == 64) ? 4 : 2;
     static constexpr int NCH = D * EB / 128;              // 128-byte column chunks per Q/K/V row
     static constexpr int CH_ELEMS = 128 / EB;             // elements per chunk
     static constexpr uint32_t QT_BYTES = BM * D * EB;     // one query sub-tile
     static constexpr uint32_t KV_BYTES = BN * D * EB;     // one K or V tile
     static constexpr uint32_t CHUNK = 128 * 128;          // 128 rows x 128 bytes
-    static constexpr uint32_t OFF_Q = 0;                  // [QB][sub-tile] query tiles
-    static constexpr uint32_t OFF_K = OFF_Q + 2 * QB * QT_BYTES;
+    static constexpr uint32_t OFF_Q = 0;                  // query tile slots
+    static constexpr uint32_t OFF_K = OFF_Q + NQ * QT_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
     static constexpr uint32_t BAR_BYTES = 384;
@@ -134,11 +138,12 @@ constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+
 constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
 
-// Query buffers per sub-tile: two where they fit in shared memory (D = 64 and
+// Query buffers: two per sub-tile where they fit in shared memory (D = 64 and
 // the 8-bit path), so that a persistent CTA loads the next item's Q while the
-// current item runs; the 16-bit D = 128 rings leave room for one.
+// current item runs; a three-tile ring for persistent 16-bit D = 128 (see
+// FwdCfg); one per sub-tile for one item per CTA.
 __host__ __device__ constexpr int query_buffers(int D, bool F8, bool PERSIST) {
-    return (PERSIST && (D == 64 || F8)) ? 2 : 1;
+    return (PERSIST && (D == 64 || F8)) ? 2 : (PERSIST ? 3 : 1);
 }
 
 // One work item: 256 query rows (two sub-tiles) of one (batch, head), and the
@@ -293,8 +298,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++nv;
                 return true;
             };
+            // three-tile ring: the q-th query tile loaded goes to slot q % 3, in the
+            // order Q_0, Q_1 of item 0, Q_0, Q_1 of item 1, ... (Q_1 only where
+            // the item has a second sub-tile), once the tile three loads earlier
+            // has been read by its item's last S
+            int qr = 0;
+            auto load_q_ring = [&](const Item &g, int t) -> bool {
+                const int slot = qr % 3, use = qr / 3;
+                if (use > 0 && !wait(B_Q_FREE + slot, (uint32_t)(use - 1) & 1u)) return false;
+                mbar_arrive_expect_tx(bar(B_Q_FULL + slot), C::QT_BYTES);
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_3d(sQ + slot * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS,
+                                g.row0 + t * C::BM, g.bh, bar(B_Q_FULL + slot), pol_q);
+                ++qr;
+                return true;
+            };
             for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
                 const Item g = item_at<WIN>(p, k);
+                if constexpr (QB == 3) {
+                    // this item's Q_0 was loaded one item ahead (below), except the first
+                    if (r == 0) ok = load_q_ring(g, 0);
+                    if (ok && g.act1) ok = load_q_ring(g, 1);
+                    if (ok) ok = load_k(g, 0);
+                    const int kn = item_index(r + 1);
+                    if (ok && kn < p.n_items) ok = load_q_ring(item_at<WIN>(p, kn), 0);
+                    for (int it = 0; ok && it < g.N; ++it) {
+                        if (it + 1 < g.N) ok = load_k(g, it + 1);
+                        if (ok) ok = load_v(g, it);
+                    }
+                    continue;
+                }
                 // Q_t of this item into buffer qn % QB, once the last S_t of the item
                 // that used the buffer before has read it
                 auto load_q = [&](int t, int &qn) -> bool {
@@ -316,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // wind down: every copy issued here has landed before the CTA may exit
+            for (int i = (qr > 3 ? qr - 3 : 0); i < qr; ++i)
+                mbar_wait_drain(bar(B_Q_FULL + i % 3), (uint32_t)(i / 3) & 1u, kDrainNs);
             for (int i = (qn0 > QB ? qn0 - QB : 0); i < qn0; ++i)
                 mbar_wait_drain(bar(B_Q_FULL + 2 * (i % QB)), (uint32_t)(i / QB) & 1u, kDrainNs);
             for (int i = (qn1 > QB ? qn1 - QB : 0); i < qn1; ++i)
@@ -351,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int sk = 0, sv = 0;       // ring stage of the next K and V tile to be read, over all items
             uint32_t kph = 0, vph = 0;
             int qn0 = 0, qn1 = 0;     // items so far in which sub-tile 0 / 1 took part
+            int qr = 0;               // three-tile ring: query tiles consumed so far
             int npv0 = 0, npv1 = 0;   // P V products so far per sub-tile (P_FULL phases)
+            uint32_t qfb0 = 0, qfb1 = 0, qfp0 = 0, qfp1 = 0;  // this item's Q_FULL barrier and phase per sub-tile
             bool ok = true;
             auto issue_s = [&](uint64_t dq, uint32_t s_tm, int stage) {
                 const uint64_t dks = dk + ((stage * C::KV_BYTES) >> 4);
@@ -380,10 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             // before an item's first S_t: its Q_t has landed
-            auto q_ready = [&](int t) {
-                const int q = t ? qn1 : qn0;  // the item's Q_t is the q-th load: buffer q % QB
-                return wait(B_Q_FULL + 2 * (q % QB) + t, (uint32_t)(q / QB) & 1u);
-            };
+            auto q_ready = [&](int t) { return wait(t ? qfb1 : qfb0, t ? qfp1 : qfp0); };
             // before an item's first P_t V: the softmax warps have read the previous item's O_t
             auto o_free = [&](int t) {
                 const int q = t ? qn1 : qn0;
@@ -393,8 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item g = item_at<WIN>(p, k);
                 const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
                 const int N = g.N;
-                // this item's query buffers, their descriptors and release barriers
-                const int qb0 = 2 * (qn0 % QB), qb1 = 2 * (qn1 % QB) + 1;
+                // this item's query buffers (slots), their descriptors and barriers:
+                // buffer q % QB of sub-tile t for its q-th item, or ring slots
+                int qb0, qb1;
+                if constexpr (QB == 3) {
+                    qb0 = qr % 3;
+                    qb1 = (qr + 1) % 3;
+                    qfp0 = (uint32_t)(qr / 3) & 1u;
+                    qfp1 = (uint32_t)((qr + 1) / 3) & 1u;
+                } else {
+                    qb0 = 2 * (qn0 % QB);
+                    qb1 = 2 * (qn1 % QB) + 1;
+                    qfp0 = (uint32_t)(qn0 / QB) & 1u;
+                    qfp1 = (uint32_t)(qn1 / QB) & 1u;
+                }
+                qfb0 = B_Q_FULL + qb0;
+                qfb1 = B_Q_FULL + qb1;
                 const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
                 const uint32_t qf0 = B_Q_FREE + qb0, qf1 = B_Q_FREE + qb1;
                 int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
@@ -477,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++qn0;
                 if (g.act1) ++qn1;
+                qr += g.act1 ? 2 : 1;
             }
             // wind down: every MMA issued here is complete before TMEM is freed
             tc_commit(bar(B_DRAIN));
