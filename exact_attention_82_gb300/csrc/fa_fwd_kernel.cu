@@ -18,9 +18,11 @@
 // sub-tiles t = 0, 1, which share every K/V tile:
 //   warps 10-11 idle (they complete the third warpgroup, whose registers go
 //              to the softmax warpgroups);
-//   warp 9     TMA producer: Q0 and Q1 of each item (as soon as the previous
-//              item's last S MMA has read the buffer), then K_j and V_j into
-//              two shared-memory rings (128-byte swizzle), K one tile ahead;
+//   warp 9     TMA producer: Q0 and Q1 of each item (as soon as the item
+//              that used the buffer before has read it with its last S MMA;
+//              with the three-tile query ring of 16-bit D = 128, the next
+//              item's Q0 a whole item ahead), then K_j and V_j into two
+//              shared-memory rings (128-byte swizzle), K one tile ahead;
 //   warp 8     allocates all 512 tensor-memory (TMEM) columns and issues the
 //              tcgen05 MMAs (the whole warp runs the issue loop, one elected
 //              lane issues each instruction), in the order
