@@ -47,7 +47,7 @@ cudaError_t launch_splitkv(int D, const CUtensorMap &tm_k, const CUtensorMap &tm
                            cudaStream_t stream);
 cudaError_t splitkv_status_read_and_clear(int *out);
 // Built-in scratch of fa_fwd_splitkv_noalloc: size, and its device address
-// on the current device (looked up on the first call per device).
+// in the current device's context (looked up on every call).
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
 cudaError_t splitkv_scratch(void **out);
 

@@ -27,8 +27,6 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "../../include/fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -251,6 +249,10 @@ __global__ void __launch_bounds__(kSkvThreads, 2)
         if (all_ok) {
             p.o_part[base * D + d] = O / L;
             if (d == 0) p.lse_part[base] = (M + lg2_approx(L)) * 0.69314718055994531f;
+        } else if (d == 0) {
+            // a wait gave up: mark this partial invalid, so the merge yields NaN
+            // rather than a blend of whatever the workspace held before
+            p.lse_part[base] = __int_as_float(0x7fc00000);
         }
     }
     __syncthreads();
@@ -324,25 +326,20 @@ cudaError_t launch_splitkv(int D, const CUtensorMap &tm_k, const CUtensorMap &tm
 // process exits, and every call on a device shares them.
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
-// Device address of the scratch array for the current device.  The first
-// call on a device looks it up (cudaGetSymbolAddress, with that device
-// current) and caches it; later calls only read the cache.  In host code the
-// array's name is just a host-side stand-in, never a device address.
+// Device address of the scratch array in the current device's context.  In
+// host code the array's name is only a host-side stand-in, never a device
+// address, so it is looked up with cudaGetSymbolAddress, with the device
+// current, on every call: after the module is loaded that is a host-side
+// table read, and nothing is cached that a context reset (cudaDeviceReset, or
+// a primary context released and created again) could leave pointing at a
+// module image that no longer exists.  The first call on a device loads the
+// library's module there (with lazy loading), so it should come before any
+// stream capture.
 cudaError_t splitkv_scratch(void **out) {
-    static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = ptr;
-    }
-    *out = addr[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 

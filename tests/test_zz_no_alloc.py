@@ -6,7 +6,9 @@ that must not take the synchronisation cudaMalloc can imply -- so this entry
 point takes no workspace.  Its results must match fa_fwd_splitkv (the same
 computation with a caller-provided workspace) within the parity tolerance,
 on two calls in a row: the second call reuses the scratch the first one
-left behind, with different sizes and a different split count.
+left behind, with different sizes and a different split count.  Small calls
+are also checked against the fp64 oracle directly, so a mistake shared by
+both CUDA entry points (a wrong offset into the scratch, say) cannot hide.
 
 This file is named to be collected last, so a run that stops at the first
 failure has run every other test before it.  It passes alone in a fresh
@@ -18,8 +20,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import exact_attention_82_gb300 as fa
-from exact_attention_82_gb300.inputs import make_qkv
+from exact_attention_82_gb300.inputs import bf16_bits, make_qkv
+from parity_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -73,3 +77,12 @@ def test_noalloc_refuses_beyond_its_scratch():
                                          lse.data_ptr(), 1, 64, 8, 16384, 128, ctypes.c_float(0.1),
                                          256, torch.cuda.current_stream().cuda_stream)
     assert st == fa.FA_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_matches_oracle_on_two_calls_in_a_row():
+    for (B, H, Sq, Sk, D, splits, seed) in [(1, 2, 3, 700, 64, 0, 44), (2, 1, 1, 1500, 128, 7, 45)]:
+        q, k, v = make_qkv(B, H, Sq, Sk, D, seed=seed)
+        og, lg = _noalloc(q.cuda(), k.cuda(), v.cuda(), splits)
+        ro, rl = oracle.attn_fwd(bf16_bits(q), bf16_bits(k), bf16_bits(v), D ** -0.5, False)
+        compare(og, lg, ro, rl, f"noalloc B{B} H{H} Sq{Sq} Sk{Sk} D{D} splits{splits}")
+    assert fa.fa_device_status() == fa.FA_OK
