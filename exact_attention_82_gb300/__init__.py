@@ -15,7 +15,7 @@ import threading
 from . import build as _build
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_strerror", "fa_device_status",
-           "fa_selftest_bounded_wait", "fa_version", "FAError", "lib", "library_path",
+           "fa_selftest_bounded_wait", "fa_selftest_fwd_timeout", "fa_version", "FAError", "lib", "library_path",
            "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
@@ -60,6 +60,8 @@ _SIGNATURES = {
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_device_status": (_i, [_vp]),
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
+    "fa_selftest_fwd_timeout": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float,
+                                     _i, ctypes.c_ulonglong, _vp]),
     "fa_version": (_i, []),
 }
 
@@ -307,3 +309,13 @@ def fa_device_status(stream=None) -> int:
 
 def fa_selftest_bounded_wait(timeout_us: int, stream=None) -> int:
     return lib().fa_selftest_bounded_wait(int(timeout_us), _stream_ptr(stream))
+
+
+def fa_selftest_fwd_timeout(q, k, v, o, lse, scale, causal, timeout_ns: int, stream=None) -> int:
+    """fa_fwd with every on-chip wait bounded by `timeout_ns` (tests of the give-up
+    path); returns the launch status.  q, k, v, o, lse: contiguous CUDA tensors."""
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    return lib().fa_selftest_fwd_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, H, Sq, Sk, D, float(scale),
+                                         int(bool(causal)), int(timeout_ns), _stream_ptr(stream))

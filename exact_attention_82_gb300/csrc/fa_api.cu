@@ -141,7 +141,8 @@ static int check_fwd(const void *q, const void *k, const void *v, const void *o,
 // Encode the maps and launch; arguments already checked.  Key j is allowed
 // for query i iff i - wl <= j <= i + wr (a negative bound: unbounded).
 static int launch_checked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
-                          int Sk, int D, float scale, int wl, int wr, void *stream) {
+                          int Sk, int D, float scale, int wl, int wr, void *stream,
+                          unsigned long long timeout_ns = kWaitLimitNs) {
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
     const long long BH = (long long)B * H;
     const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
@@ -163,7 +164,7 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.wr = wr < 0 ? -1 : wr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.o_scale = 1.f;
-    p.timeout_ns = kWaitLimitNs;
+    p.timeout_ns = timeout_ns;
     const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
@@ -238,7 +239,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
 }
 
 // ------------------------------------------------------------- split-KV path
-// Keys per split for `splits` ranges: a multiple of the 128-key tile.
+// Keys per split for `splits` ranges: a multiple of the 64-key split tile.
 static int split_chunk(int Sk, int splits) {
     const int per = (Sk + splits - 1) / splits;
     return ((per + fa::kSplitTileKeys - 1) / fa::kSplitTileKeys) * fa::kSplitTileKeys;
@@ -412,4 +413,15 @@ extern "C" int fa_selftest_bounded_wait(int timeout_us, void *stream) {
     const cudaError_t e = fa::launch_wait_selftest((unsigned long long)timeout_us * 1000ull, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
+}
+
+extern "C" int fa_selftest_fwd_timeout(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                       int H, int Sq, int Sk, int D, float scale, int causal,
+                                       unsigned long long timeout_ns, void *stream) {
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (causal != 0 && causal != 1) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (causal && Sq != Sk) return FA_ERR_UNSUPPORTED_CAUSAL;
+    if (timeout_ns > kWaitLimitNs) return FA_ERR_BAD_SHAPE;
+    return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, -1, causal ? 0 : -1, stream, timeout_ns);
 }

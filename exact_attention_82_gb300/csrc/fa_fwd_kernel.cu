@@ -41,13 +41,18 @@
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
 // the first 64 columns of S_t (128 bf16 packed in pairs).
 //
-// The running max is only moved when a row's max grows by more than 2^8 (in
-// exp2 units): P and l keep using the stale max, which is exact because O and
-// l are divided by the same factor at the end, and it takes the O rescale off
-// almost every iteration ("reduce non-matmul work", same page, section
-// "第四处差异：v2 减少非 matmul 开销").  O_t is stable while sub-tile t is
-// between "S_t full" and "P_t full" (S_t is issued after the previous P_t V),
-// so the softmax thread rescales its own O row there when needed.
+// The row max is taken on a sub-tile's first key tile only (16-bit path);
+// later tiles compute P against that stale max, which is exact because O and
+// l are relative to the same max and divided at the end, and it takes the
+// max pass and the O rescale off almost every iteration ("reduce non-matmul
+// work", same page, section "第四处差异：v2 减少非 matmul 开销").  A tile is
+// redone against its true max (and O and l rescaled) only when its row sum
+// exceeds 2^64 or is not finite, i.e. when a score has grown more than 64
+// (exp2 units) past the max in use.  The 8-bit path takes the row max every
+// tile and moves the running max when it is exceeded by more than 2 (P must
+// fit e4m3).  O_t is stable while sub-tile t is between "S_t full" and
+// "P_t full" (S_t is issued after the previous P_t V), so the softmax thread
+// rescales its own O row there when needed.
 //
 // Key tiles run from the last one to the first, so the only tile of a
 // sub-tile that needs masking (causal diagonal or ragged last tile) is its

@@ -154,7 +154,9 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
  *
  * Errors: those of fa_fwd (causal does not apply), FA_ERR_BAD_SHAPE for
  * Sq > 8, B*H > 65535 or num_splits > 256, FA_ERR_WORKSPACE for a missing,
- * misaligned or short workspace.  Deterministic; no atomics.
+ * misaligned or short workspace.  Deterministic; no atomics.  If an on-chip
+ * wait gives up (fa_device_status then returns FA_ERR_TIMEOUT), the affected
+ * partials are marked invalid and the merged O and LSE of their rows are NaN.
  */
 int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                    int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
@@ -181,13 +183,16 @@ int fa_splitkv_num_splits(int B, int H, int Sq, int Sk, int D);
  * GPU that loads the library holds it until the process exits).
  *
  * Arguments and results are those of fa_fwd_splitkv without the workspace;
- * the caller still provides q, k, v, o and lse.  The first call on a device
- * looks up the array's device address for that device (cudaGetSymbolAddress)
- * and caches it, so make that first call before any stream capture.  All
+ * the caller still provides q, k, v, o and lse.  Every call looks up the
+ * array's device address in the current device's context
+ * (cudaGetSymbolAddress); the first call on a device also loads the library's
+ * module there, so make that first call before any stream capture.  All
  * calls on a device share the one array and it keeps the last call's bytes;
- * nothing in it needs to start at zero (each call writes every partial result
- * before reading it).  Calls whose kernels overlap on the GPU (two streams,
- * or two host threads) race on the array: serialise them.
+ * nothing in it needs to start at zero (each call's partial kernel writes
+ * every partial result before its merge kernel reads it; after a wait that
+ * gave up, the partials it could not finish are marked invalid, as for
+ * fa_fwd_splitkv).  Calls whose kernels overlap on the GPU (two streams, or
+ * two host threads) race on the array: serialise them.
  * Errors: those of fa_fwd_splitkv, plus FA_ERR_SCRATCH_LIMIT when the sizes
  * need more than 16 MiB of scratch (fa_fwd_splitkv_workspace_bytes tells the
  * need; pass a workspace to fa_fwd_splitkv for larger problems).
@@ -244,6 +249,24 @@ int fa_device_status(void *stream);
  * is involved: this exists so tests can show the give-up path works.
  */
 int fa_selftest_bounded_wait(int timeout_us, void *stream);
+
+/*
+ * fa_selftest_fwd_timeout -- fa_fwd with every on-chip wait of the forward
+ * kernel bounded by `timeout_ns` (0 .. 2e9) instead of the 2 s that fa_fwd
+ * uses.  With a limit shorter than a tile load (0 gives up at the first wait
+ * that is not already satisfied), the kernel's own give-up path runs: the
+ * wait raises the CTA's abort flag and records FA_ERR_TIMEOUT in the status
+ * word, the other roles stop at their next wait, the producer waits (bounded,
+ * 20 ms) for the copies it issued, the MMA issuer for its MMAs, TMEM is freed
+ * and the CTA returns -- no trap, fault or hang.  O and LSE are then
+ * undefined.  Arguments, checks and errors are fa_fwd's, plus
+ * FA_ERR_BAD_SHAPE for timeout_ns above 2e9.  The surveyed pages have no
+ * counterpart: it exists so tests can show the forward kernel winds down
+ * cleanly and leaves the context usable.
+ */
+int fa_selftest_fwd_timeout(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                            unsigned long long timeout_ns, void *stream);
 
 /* fa_version -- library version, major*10000 + minor*100 + patch. */
 int fa_version(void);

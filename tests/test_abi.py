@@ -96,6 +96,11 @@ def test_alias():
 
 
 def test_selftest_argument_check():
+    st = fa.lib().fa_selftest_fwd_timeout(A, A2, A3, A4, A5, 1, 1, 128, 128, 64, 0.125, 0,
+                                          2_000_000_001, 0)
+    assert st == fa.FA_ERR_BAD_SHAPE  # wait limit above 2 s
+    st = fa.lib().fa_selftest_fwd_timeout(None, A2, A3, A4, A5, 1, 1, 128, 128, 64, 0.125, 0, 0, 0)
+    assert st == fa.FA_ERR_NULLPTR
     assert fa.fa_selftest_bounded_wait(0, stream=0) == fa.FA_ERR_BAD_SHAPE
     assert fa.fa_selftest_bounded_wait(2_000_000, stream=0) == fa.FA_ERR_BAD_SHAPE
 

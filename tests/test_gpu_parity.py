@@ -164,6 +164,29 @@ def test_bounded_wait_gives_up_and_reports():
     full_parity(1, 1, 128, 128, 64, False, seed=1)  # context still works
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_kernel_gives_up_cleanly(D):
+    """The attention kernel's own give-up path, on one CTA's worth of work (one
+    item of 256 query rows): with every wait limited to 0 ns, the first wait in
+    progress when the global timer ticks gives up, raises the CTA's abort flag
+    and records FA_ERR_TIMEOUT; the other roles stop, the producer and the MMA
+    issuer wait (bounded) for their copies and MMAs in flight, TMEM is freed and
+    the kernel returns.  The key sequence is long (65,536 keys, about a
+    millisecond of tile waits), so that a timer tick falls inside some wait
+    whatever the timer's resolution.  A normal call after it must pass parity,
+    so the context is still usable."""
+    assert fa.fa_device_status() == fa.FA_OK
+    q, k, v = make_qkv(1, 1, 256, 65536, D, seed=31)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 256), dtype=torch.float32, device="cuda")
+    assert fa.fa_selftest_fwd_timeout(q, k, v, o, lse, D ** -0.5, False, 0) == fa.FA_OK
+    assert fa.fa_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_device_status() == fa.FA_OK  # cleared by the read
+    full_parity(1, 2, 300, 300, D, True, seed=32)
+    assert fa.fa_device_status() == fa.FA_OK
+
+
 def _growing_scores(D, lift, causal):
     """Keys of the first key tile (index 0, processed last) score `lift` (in
     exp2 units) above every other key, so later tiles outgrow the max taken
