@@ -9,11 +9,15 @@ bf16 tensor peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-For N > 1 it runs under torch.distributed.run, one rank per GPU; every rank
-processes its own full workload (independent problems, no data-path
-collective: weak scaling) and value = all ranks' FLOPs / the slowest rank's
-time.  `--impl reference` times the fp64 CPU oracle on the host cores on a
-bounded sample of the same workload (rank 0 only).
+For N > 1 it runs one rank per GPU under torch.distributed.run (started by
+the caller, or by bench.py itself when --gpus N > 1 is given without a
+WORLD_SIZE in the environment).  By default every rank processes its own full
+workload (independent problems, no data-path collective: weak scaling); with
+--split heads the B*H heads of ONE workload are dealt out to the ranks in
+contiguous blocks, each rank writing only its heads' rows of O and LSE (strong
+scaling).  Either way value = all ranks' FLOPs / the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -58,6 +62,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target seconds of oracle work for the CPU baseline")
+    ap.add_argument("--split", choices=["none", "heads"], default="none",
+                    help="none: every rank runs the whole workload (weak scaling); heads: the "
+                         "B*H heads of one workload are split across the ranks (strong scaling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -117,6 +124,39 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 def whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
     """Every rank processes its own full workload: all ranks' FLOPs / the slowest time."""
     return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+def rank_workload(w, world: int, rank: int, split: str):
+    """The part of workload `w` this rank runs, and the heads it owns:
+    (workload, start, count).  With split "heads" the rank runs heads
+    [start, start + count) of the flattened B*H axis as a B = 1, H = count
+    workload; otherwise the whole workload (start 0, count B*H)."""
+    import dataclasses
+
+    from exact_attention_82_gb300.shard import head_range
+
+    if split != "heads":
+        return w, 0, w.B * w.H
+    start, count = head_range(w.B * w.H, world, rank)
+    return dataclasses.replace(w, B=1, H=count), start, count
+
+
+def spawn_command(argv, nproc: int, port: int):
+    """The command that runs this script as `nproc` ranks on this node under
+    torch.distributed.run (rendezvous on 127.0.0.1), with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr=127.0.0.1", f"--master-port={port}",
+            os.path.abspath(__file__), *argv]
+
+
+def _free_port() -> int:
+    import socket
+
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
 
 
 # ----------------------------------------------------------------- clocks
@@ -231,10 +271,18 @@ def run_ours(args, rank, world, local_rank):
     import exact_attention_82_gb300 as fa
     from exact_attention_82_gb300.inputs import WORKLOADS
 
-    w = WORKLOADS[args.workload]
+    from exact_attention_82_gb300.shard import head_slice
+
+    w_full = WORKLOADS[args.workload]
+    # this rank's part: the whole workload, or (--split heads) its block of heads
+    w, h0, nh = rank_workload(w_full, world, rank, args.split)
+    if args.split == "heads" and w_full.path not in ("fwd", "fp8"):
+        raise SystemExit("--split heads applies to the forward workloads")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     q, k, v, descales = workload_inputs(args.workload)
+    if args.split == "heads":
+        q, k, v = (head_slice(t, h0, nh).contiguous() for t in (q, k, v))
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
@@ -244,7 +292,8 @@ def run_ours(args, rank, world, local_rank):
     ws = make_workspace(fa, w, dq, dk, dv, dev, descales)
 
     def step():
-        run_path(fa, w, dq, dk, dv, o, lse, ws, stream)
+        if nh > 0:  # a rank beyond the head count has nothing to do
+            run_path(fa, w, dq, dk, dv, o, lse, ws, stream)
 
     def barrier():
         if world > 1:
@@ -277,7 +326,9 @@ def run_ours(args, rank, world, local_rank):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status after timing: {fa.fa_strerror(st)}")
 
-    e2e = None if args.no_e2e else run_e2e(args, w, q, k, v, dev, world, descales)
+    strong = args.split == "heads"
+    e2e = None if args.no_e2e else run_e2e(args, w, q, k, v, dev, world, descales,
+                                           job_flops=w_full.flops if strong else None)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q, k, v, args.cpu_seconds, descales)
@@ -286,8 +337,17 @@ def run_ours(args, rank, world, local_rank):
     peaks, which = measured_peaks()
     peak = float(peaks["bf16_tflops"]) if peaks else FALLBACK_PEAK_TFLOPS
     tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
-    value = whole_job_tflops(w.flops, world, ms)
+    # strong: the ranks share one workload; weak: each runs a whole one
+    value = (w_full.flops / (ms * 1e-3) / 1e12) if strong else whole_job_tflops(w.flops, world, ms)
+    if strong:
+        parallelism = (f"B*H = {w_full.B * w_full.H} heads of one workload split across {world} "
+                       f"GPU(s) in contiguous blocks (rank 0: heads [{h0}, {h0 + nh})), each "
+                       f"writing only its heads' O and LSE; no data-path collective")
+    else:
+        parallelism = f"independent workload per GPU x{world}"
     traffic = traffic_per_launch(w)
+    if traffic is not None and strong:  # recorded for the whole workload; this rank runs nh heads
+        traffic = traffic * nh / (w_full.B * w_full.H)
     if w.path == "splitkv":
         # decode reads each key and value once: bound by HBM bandwidth
         hbm_peak = float(peaks["hbm_gbs"]) if peaks else FALLBACK_HBM_GBS
@@ -313,11 +373,11 @@ def run_ours(args, rank, world, local_rank):
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong" if strong else "weak", "vs_baseline": None,
         "dtype": "e4m3" if w.path == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "desc": w.describe(), "B": w.B, "H": w.H, "Sq": w.Sq,
-                   "Sk": w.Sk, "D": w.D, "causal": w.causal, "window": list(w.window),
-                   "parallelism": f"independent workload per GPU x{world}",
+        "config": {"workload": w_full.name, "desc": w_full.describe(), "B": w_full.B,
+                   "H": w_full.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "causal": w.causal,
+                   "window": list(w.window), "parallelism": parallelism,
                    "l2": "flushed before every step (256 MiB write outside the timed events)",
                    "pct_of_bf16_peak": round(100.0 * tflops_launch / peak, 2),
                    "ms_median": round(statistics.median(times), 5), "ms_min": round(min(times), 5),
@@ -327,13 +387,13 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if w.path in ("splitkv", "bwd") else 1),
+        "gpu_launches": args.steps * (2 if w.path in ("splitkv", "bwd") else 1) * (nh > 0),
         "clocks": clk,
         "impl": "ours",
     }
 
 
-def _pipelined_e2e(args, host_in, host_out, launch, dev, world, flops):
+def _pipelined_e2e(args, host_in, host_out, launch, dev, world, flops, job_flops=None):
     """End-to-end steps through the public call: step i copies `host_in` (pinned)
     to the device, calls `launch(dev_in, dev_out, stream)` and reads `dev_out`
     back into `host_out` (pinned).  Steps are pipelined as a serving loop runs
@@ -394,7 +454,8 @@ def _pipelined_e2e(args, host_in, host_out, launch, dev, world, flops):
         dist.barrier()
     steps = max(3, min(args.steps, 50))
     ms = max_over_ranks(run(steps) / steps, world, dev)
-    return {"value": round(whole_job_tflops(flops, world, ms), 2), "unit": "TFLOP/s",
+    value = job_flops / (ms * 1e-3) / 1e12 if job_flops else whole_job_tflops(flops, world, ms)
+    return {"value": round(value, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": steps,
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out),
@@ -402,10 +463,11 @@ def _pipelined_e2e(args, host_in, host_out, launch, dev, world, flops):
                        "(three streams, two device buffer sets)"}
 
 
-def run_e2e(args, w, q, k, v, dev, world, descales=None):
+def run_e2e(args, w, q, k, v, dev, world, descales=None, job_flops=None):
     """Same metric through the public call with host buffers: every step copies
     Q, K, V from pinned host memory, runs the attention call and reads O and LSE
-    back (pipelined across steps, see _pipelined_e2e)."""
+    back (pipelined across steps, see _pipelined_e2e).  With `job_flops` (a head
+    split) the ranks share one workload of that many FLOPs."""
     import torch
 
     import exact_attention_82_gb300 as fa
@@ -418,9 +480,10 @@ def run_e2e(args, w, q, k, v, dev, world, descales=None):
     ws = make_workspace(fa, w, *host_in, dev, descales)  # (Q, K, V only matter on the backward path)
 
     def launch(din, dout, stream):
-        run_path(fa, w, *din, *dout, ws, stream)
+        if w.B * w.H > 0:
+            run_path(fa, w, *din, *dout, ws, stream)
 
-    return _pipelined_e2e(args, host_in, host_out, launch, dev, world, w.flops)
+    return _pipelined_e2e(args, host_in, host_out, launch, dev, world, w.flops, job_flops)
 
 
 def run_e2e_bwd(args, w, q, k, v, dev, world):
@@ -632,9 +695,13 @@ def main(argv=None):
             return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # asked for N GPUs without a launcher: start the N ranks here
+        return subprocess.call(spawn_command(sys.argv[1:] if argv is None else list(argv),
+                                             args.gpus, _free_port()))
     if world != args.gpus:
-        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
-              file=sys.stderr)
+        print(f"error: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if world > 1:
         import torch.distributed as dist
 
