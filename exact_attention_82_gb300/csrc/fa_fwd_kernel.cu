@@ -39,7 +39,11 @@
 //              a CTA with one item through shared memory and a TMA store)
 //              and LSE.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
-// the first 64 columns of S_t (128 bf16 packed in pairs).
+// the first 64 columns of S_t (128 bf16 packed in pairs) -- except at 16-bit
+// D = 64, where the 128 columns O leaves free hold P0 and P1 on their own
+// [384,448) [448,512): the next S_t is then issued as soon as the softmax has
+// read S_t, instead of after P_t V has consumed P_t, and an item's O epilogue
+// is deferred to the next item's first tile (see SEPP below).
 //
 // The row max is taken on a sub-tile's first key tile only (16-bit path);
 // later tiles compute P against that stale max, which is exact because O and
@@ -98,6 +102,11 @@ struct FwdCfg {
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256;
+    // 16-bit D = 64 leaves 128 TMEM columns free: P_t gets its own 64 there
+    // instead of overwriting S_t, so the next S_t can be issued as soon as
+    // the softmax has read S_t (not only after P_t V has consumed P_t)
+    static constexpr bool SEPP = D == 64 && !F8;
+    static constexpr uint32_t TM_P = TM_O + 2 * D;  // SEPP: P_t at TM_P + 64 t
     // one MMA takes 32 bytes of the contraction: 16 bf16 or 32 e4m3 elements
     static constexpr int S_STEPS = D * EB / 32;
     static constexpr int PV_STEPS = BN * EB / 32;
@@ -133,6 +142,8 @@ enum : uint32_t {
     B_O_DONE = 28,   // + sub-tile: the item's last P_t V is complete
     B_O_FREE = 30,   // + sub-tile: the softmax warps have read O_t out (128 arrivals)
     B_DRAIN = 32,
+    B_S_FREE = 33,   // + sub-tile (separate P): the softmax warps have read S_t (128 arrivals)
+    B_PV_DONE = 35,  // + sub-tile (separate P): a P_t V product is complete
 };
 constexpr uint32_t SLOT_TMEM = 320;   // byte offset of the TMEM base address
 constexpr uint32_t SLOT_ABORT = 324;  // byte offset of the abort flag
@@ -254,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_O_FREE + t), 128);
         }
         mbar_init(bar(B_DRAIN), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_S_FREE + t), 128);
+            mbar_init(bar(B_PV_DONE + t), 1);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -430,109 +445,200 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q = t ? qn1 : qn0;
                 return q == 0 || wait(B_O_FREE + t, (uint32_t)(q - 1) & 1u);
             };
-            for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
-                const Item g = item_at<WIN>(p, k);
-                const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
-                const int N = g.N;
-                // this item's query buffers (slots), their descriptors and barriers:
-                // buffer q % QB of sub-tile t for its q-th item, or ring slots
-                int qb0, qb1;
-                if constexpr (QB == 3) {
-                    qb0 = qr % 3;
-                    qb1 = (qr + 1) % 3;
-                    qfp0 = (uint32_t)(qr / 3) & 1u;
-                    qfp1 = (uint32_t)((qr + 1) / 3) & 1u;
-                } else {
-                    qb0 = 2 * (qn0 % QB);
-                    qb1 = 2 * (qn1 % QB) + 1;
+            if constexpr (C::SEPP) {
+                // P in its own TMEM columns (16-bit D = 64).  Per key tile: S0_j and
+                // S1_j, each as soon as the softmax has read the previous S_t
+                // (S_FREE), then the P V products of the previous key tile -- so
+                // that, across an item boundary too, the next S runs while this
+                // item's last softmax is still computing.  (Issuing each sub-tile's
+                // S and previous P V together, S0 PV0 S1 PV1, measured slower.)
+                // Each P_t V product
+                // commits PV_DONE_t, after which the softmax may overwrite P_t,
+                // rescale O_t or (after an item's last product) read O_t out.  The
+                // softmax reads an item's O_t before it signals the next item's
+                // first P_t, and that product (which overwrites O_t) waits for the
+                // signal, so O needs no hand-over barrier of its own.
+                int ns0 = 0, ns1 = 0;  // S_t issued so far, over all items (S_FREE phases)
+                struct PendingPV {     // a sub-tile's P V product still to issue (previous key tile)
+                    bool on, first;
+                    int stage;
+                    uint32_t phase;
+                } pd0 = {false, false, 0, 0u}, pd1 = {false, false, 0, 0u};
+                bool vpend = false;    // the previous key tile's V stage is still to be released
+                int svp = 0;
+                auto pv_sepp = [&](int t, bool first, int stage, uint32_t phase) -> bool {
+                    int &npv = t ? npv1 : npv0;
+                    if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                    if (!wait(B_V_FULL + stage, phase)) return false;
+                    tc_fence_after();
+                    const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                        tc_mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_P + t * 64 + kk * 8,
+                                  dvs + ((kk * C::V_STEP) >> 4), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(B_PV_DONE + t));
+                    ++npv;
+                    return true;
+                };
+                auto flush_pv = [&](int t, PendingPV &pd) -> bool {
+                    if (!pd.on) return true;
+                    pd.on = false;
+                    return pv_sepp(t, pd.first, pd.stage, pd.phase);
+                };
+                for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
+                    const Item g = item_at<WIN>(p, k);
+                    const int qb0 = 2 * (qn0 % QB), qb1 = 2 * (qn1 % QB) + 1;
+                    qfb0 = B_Q_FULL + qb0;
+                    qfb1 = B_Q_FULL + qb1;
                     qfp0 = (uint32_t)(qn0 / QB) & 1u;
                     qfp1 = (uint32_t)(qn1 / QB) & 1u;
-                }
-                qfb0 = B_Q_FULL + qb0;
-                qfb1 = B_Q_FULL + qb1;
-                const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
-                const uint32_t qf0 = B_Q_FREE + qb0, qf1 = B_Q_FREE + qb1;
-                int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
-                {
-                    // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
-                    int svp = 0;          // V stage of the previous tile
-                    uint32_t vpph = 0;
-                    auto issue_pv = [&](int t, int ipv, int stage, uint32_t phase) -> bool {
-                        int &npv = t ? npv1 : npv0;
-                        if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
-                        if (!wait(B_V_FULL + stage, phase)) return false;
-                        if constexpr (PERSIST) {
-                            if (ipv == 0 && !o_free(t)) return false;
-                        }
-                        tc_fence_after();
-                        issue_pv_mma(t, ipv > 0, stage);
-                        ++npv;
-                        return true;
-                    };
-                    if constexpr (!PERSIST) ok = q_ready(0) && (!g.act1 || q_ready(1));
-                    for (int it = 0; ok && it < N; ++it) {
+                    const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
+                    for (int it = 0; ok && it < g.N; ++it) {
                         ok = wait(B_K_FULL + sk, kph);
                         if (!ok) break;
-                        tc_fence_after();
-                        const bool p0 = it >= first0 && it <= last0;
-                        const bool p1 = it >= first1 && it <= last1;
+                        const bool p0 = it >= g.first[0] && it <= g.last[0];
+                        const bool p1 = it >= g.first[1] && it <= g.last[1];
                         if (p0) {
-                            if constexpr (PERSIST) {
-                                if (it == first0) {
-                                    ok = q_ready(0);
-                                    if (!ok) break;
-                                    tc_fence_after();
-                                }
-                            }
+                            if (it == g.first[0]) ok = q_ready(0);
+                            if (ok && ns0 > 0) ok = wait(B_S_FREE + 0, (uint32_t)(ns0 - 1) & 1u);
+                            if (!ok) break;
+                            tc_fence_after();
                             issue_s(dq0, tmem, sk);
                             tc_commit(bar(B_S_FULL + 0));
-                            if constexpr (PERSIST) {
-                                if (it == last0) tc_commit(bar(qf0));
-                            }
-                        }
-                        if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
-                            ok = issue_pv(1, ipv1++, svp, vpph);
-                            if (!ok) break;
-                            if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
-                            tc_commit(bar(B_V_EMPTY + svp));
+                            ++ns0;
+                            if (it == g.last[0]) tc_commit(bar(B_Q_FREE + qb0));
                         }
                         if (p1) {
-                            if constexpr (PERSIST) {
-                                if (it == first1) {
-                                    ok = q_ready(1);
-                                    if (!ok) break;
-                                    tc_fence_after();
-                                }
-                            }
+                            if (it == g.first[1]) ok = q_ready(1);
+                            if (ok && ns1 > 0) ok = wait(B_S_FREE + 1, (uint32_t)(ns1 - 1) & 1u);
+                            if (!ok) break;
+                            tc_fence_after();
                             issue_s(dq1, tmem + 128, sk);
                             tc_commit(bar(B_S_FULL + 1));
-                            if constexpr (PERSIST) {
-                                if (it == last1) tc_commit(bar(qf1));
-                            }
+                            ++ns1;
+                            if (it == g.last[1]) tc_commit(bar(B_Q_FREE + qb1));
                         }
                         tc_commit(bar(B_K_EMPTY + sk));
-                        if (p0) {
-                            ok = issue_pv(0, ipv0++, sv, vph);
-                            if (!ok) break;
-                            if (it == last0) tc_commit(bar(B_O_DONE + 0));
-                            if (!p1) tc_commit(bar(B_V_EMPTY + sv));
-                        }
-                        if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                        ok = flush_pv(0, pd0) && flush_pv(1, pd1);
+                        if (!ok) break;
+                        if (vpend) tc_commit(bar(B_V_EMPTY + svp));  // both products of that tile are issued
+                        pd0 = {p0, it == g.first[0], sv, vph};
+                        pd1 = {p1, it == g.first[1], sv, vph};
+                        vpend = true;
                         svp = sv;
-                        vpph = vph;
+                        if (++sk == C::KST) { sk = 0; kph ^= 1u; }
                         if (++sv == C::VST) { sv = 0; vph ^= 1u; }
                     }
-                    if (ok && last1 == N - 1) {
-                        ok = issue_pv(1, ipv1, svp, vpph);
-                        if (ok) {
-                            tc_commit(bar(B_O_DONE + 1));
-                            tc_commit(bar(B_V_EMPTY + svp));
+                    ++qn0;
+                    if (g.act1) ++qn1;
+                }
+                if (ok) ok = flush_pv(0, pd0) && flush_pv(1, pd1);
+                if (ok && vpend) tc_commit(bar(B_V_EMPTY + svp));
+            } else {
+                for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
+                    const Item g = item_at<WIN>(p, k);
+                    const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
+                    const int N = g.N;
+                    // this item's query buffers (slots), their descriptors and barriers:
+                    // buffer q % QB of sub-tile t for its q-th item, or ring slots
+                    int qb0, qb1;
+                    if constexpr (QB == 3) {
+                        qb0 = qr % 3;
+                        qb1 = (qr + 1) % 3;
+                        qfp0 = (uint32_t)(qr / 3) & 1u;
+                        qfp1 = (uint32_t)((qr + 1) / 3) & 1u;
+                    } else {
+                        qb0 = 2 * (qn0 % QB);
+                        qb1 = 2 * (qn1 % QB) + 1;
+                        qfp0 = (uint32_t)(qn0 / QB) & 1u;
+                        qfp1 = (uint32_t)(qn1 / QB) & 1u;
+                    }
+                    qfb0 = B_Q_FULL + qb0;
+                    qfb1 = B_Q_FULL + qb1;
+                    const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
+                    const uint32_t qf0 = B_Q_FREE + qb0, qf1 = B_Q_FREE + qb1;
+                    int ipv0 = 0, ipv1 = 0;  // P V products of this item per sub-tile
+                    {
+                        // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
+                        int svp = 0;          // V stage of the previous tile
+                        uint32_t vpph = 0;
+                        auto issue_pv = [&](int t, int ipv, int stage, uint32_t phase) -> bool {
+                            int &npv = t ? npv1 : npv0;
+                            if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                            if (!wait(B_V_FULL + stage, phase)) return false;
+                            if constexpr (PERSIST) {
+                                if (ipv == 0 && !o_free(t)) return false;
+                            }
+                            tc_fence_after();
+                            issue_pv_mma(t, ipv > 0, stage);
+                            ++npv;
+                            return true;
+                        };
+                        if constexpr (!PERSIST) ok = q_ready(0) && (!g.act1 || q_ready(1));
+                        for (int it = 0; ok && it < N; ++it) {
+                            ok = wait(B_K_FULL + sk, kph);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const bool p0 = it >= first0 && it <= last0;
+                            const bool p1 = it >= first1 && it <= last1;
+                            if (p0) {
+                                if constexpr (PERSIST) {
+                                    if (it == first0) {
+                                        ok = q_ready(0);
+                                        if (!ok) break;
+                                        tc_fence_after();
+                                    }
+                                }
+                                issue_s(dq0, tmem, sk);
+                                tc_commit(bar(B_S_FULL + 0));
+                                if constexpr (PERSIST) {
+                                    if (it == last0) tc_commit(bar(qf0));
+                                }
+                            }
+                            if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
+                                ok = issue_pv(1, ipv1++, svp, vpph);
+                                if (!ok) break;
+                                if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                                tc_commit(bar(B_V_EMPTY + svp));
+                            }
+                            if (p1) {
+                                if constexpr (PERSIST) {
+                                    if (it == first1) {
+                                        ok = q_ready(1);
+                                        if (!ok) break;
+                                        tc_fence_after();
+                                    }
+                                }
+                                issue_s(dq1, tmem + 128, sk);
+                                tc_commit(bar(B_S_FULL + 1));
+                                if constexpr (PERSIST) {
+                                    if (it == last1) tc_commit(bar(qf1));
+                                }
+                            }
+                            tc_commit(bar(B_K_EMPTY + sk));
+                            if (p0) {
+                                ok = issue_pv(0, ipv0++, sv, vph);
+                                if (!ok) break;
+                                if (it == last0) tc_commit(bar(B_O_DONE + 0));
+                                if (!p1) tc_commit(bar(B_V_EMPTY + sv));
+                            }
+                            if (++sk == C::KST) { sk = 0; kph ^= 1u; }
+                            svp = sv;
+                            vpph = vph;
+                            if (++sv == C::VST) { sv = 0; vph ^= 1u; }
+                        }
+                        if (ok && last1 == N - 1) {
+                            ok = issue_pv(1, ipv1, svp, vpph);
+                            if (ok) {
+                                tc_commit(bar(B_O_DONE + 1));
+                                tc_commit(bar(B_V_EMPTY + svp));
+                            }
                         }
                     }
+                    ++qn0;
+                    if (g.act1) ++qn1;
+                    qr += g.act1 ? 2 : 1;
                 }
-                ++qn0;
-                if (g.act1) ++qn1;
-                qr += g.act1 ? 2 : 1;
             }
             // wind down: every MMA issued here is complete before TMEM is freed
             tc_commit(bar(B_DRAIN));
@@ -546,9 +652,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + t * 128;
         const uint32_t o_tm = tmem + lane_off + C::TM_O + t * D;
+        const uint32_t p_tm = tmem + lane_off + C::TM_P + t * 64;  // separate P only
         const float sl2 = p.scale_log2;
         int ns = 0;  // S_t tiles so far, over all items (S_FULL phases)
         int od = 0;  // items so far in which this sub-tile took part (O_DONE phases)
+        int npv = 0; // separate P: P_t tiles handed over so far (PV_DONE phases)
+        // Separate P: an item's O epilogue is deferred until the next item's
+        // first P_t is computed, so the O read sits beside that tile's work and
+        // the global stores come after its P is handed over.
+        bool pend = false;
+        float pm = 0.f, pl = 1.f;
+        int prow = 0, pbh = 0;
+        // O / l -> bf16 -> row `rg` of head `bh` in global memory (16-byte
+        // stores), and LSE; rows >= Sq are not written
+        auto store_row = [&](const uint32_t (&o)[D / 32][32], float m, float l, int rg, int bh) {
+            if (rg >= p.Sq) return;
+            // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
+            const float inv_l = (F8 ? p.o_scale : 1.f) / l;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + ((size_t)bh * p.Sq + rg) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {  // 16-byte unit (8 columns) c * 4 + u of the row
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(o[c][u * 8 + 2 * e]) * inv_l,
+                                           __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
+                    dst[c * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            p.lse[(size_t)bh * p.Sq + rg] = (m - (F8 ? kF8PShift : 0.f) + lg2_approx(l)) * 0.69314718055994531f;
+        };
         // With one item per CTA (not PERSIST) and 16-bit inputs, O is staged in
         // this sub-tile's Q buffer, free once the item's MMAs are done, and
         // written by a TMA store after the loop; a persistent CTA stores each
@@ -596,7 +730,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e < lim_lo || c * 32 + e >= lim_hi) s[c][e] = __float_as_uint(-INFINITY);
                 };
-                if (masked) apply_mask();
+                // Separate P (16-bit D = 64), full or causal attention: only the
+                // right bound lim_hi cuts a row (k_lo = 0 <= col0), so each
+                // 32-column chunk is, for the whole warp, either kept, cut partway
+                // (masked element by element) or wholly past every row's bound --
+                // then it is skipped (P = 0 there, and it takes no part in the max
+                // or the sum).  On a causal diagonal tile a warp's 32 rows cut only
+                // its own chunk.  (At D = 128 the extra code measured slower.)
+                bool skip[4] = {false, false, false, false};
+                auto mask_tile = [&]() {
+                    if constexpr (WIN || F8 || !C::SEPP) {
+                        apply_mask();
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            skip[c] = __all_sync(0xffffffffu, lim_hi <= c * 32);
+                            if (!skip[c] && !__all_sync(0xffffffffu, lim_hi >= c * 32 + 32)) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    if (c * 32 + e >= lim_hi) s[c][e] = __float_as_uint(-INFINITY);
+                            }
+                        }
+                    }
+                };
+                if (masked) mask_tile();
                 if constexpr (F8) {
                     // The tile's row max every tile; the running max moves only when
                     // it is exceeded by more than kF8Lazy, and O is then rescaled.
@@ -671,28 +828,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto take_max = [&]() {
                         // row max: four independent chains of three-input max
                         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-    #pragma unroll
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (skip[c]) continue;
+#pragma unroll
                             for (int e = 0; e < 32; e += 8)
-    #pragma unroll
+#pragma unroll
                                 for (int q = 0; q < 4; ++q)
                                     mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
                                                   __uint_as_float(s[c][e + 2 * q + 1]));
+                        }
                         const float m_new = fmaxf(m_used, max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2);
                         // 0 on a row's first keys; 1 while a row has seen no allowed key
                         alpha = (WIN && m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
                         m_used = m_new;
                     };
-                    auto exp_pass = [&]() {
+                    // use_skip: honour skipped chunks (a masked tile of full or causal
+                    // attention); every other tile takes the straight-line pass
+                    auto exp_pass = [&](bool use_skip) {
                         // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
                         // row sum in four packed partial sums
                         const float nm = (WIN && m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
                         const uint64_t nm2 = f2_pack(nm, nm);
                         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-    #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-    #pragma unroll
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (use_skip && skip[c]) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) pk[c * 16 + e] = 0u;
+                                continue;
+                            }
+#pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 float x0, x1;
                                 f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
@@ -703,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
                                 pk[c * 16 + e] = pack_bf16x2(p0, p1);
                             }
+                        }
                         float a0, a1, b0, b1;
                         f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
                         f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
@@ -711,20 +878,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the max is taken while any row of the warp has no allowed key
                     // yet (always on the first tile)
                     const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
+                    const bool skips = C::SEPP && !WIN && masked;
                     if (took_max) take_max();
-                    exp_pass();
+                    if (skips)
+                        exp_pass(true);
+                    else
+                        exp_pass(false);
                     const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
                     if (redo) {
-    #pragma unroll
+#pragma unroll
                         for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
-    #pragma unroll
+#pragma unroll
                         for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-                        if (masked) apply_mask();
+                        if (masked) mask_tile();
                         take_max();
-                        exp_pass();
+                        exp_pass(false);  // a redo is never on a masked tile of full or causal attention
                     }
-    #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_st16(s_tm + c * 16, &pk[c * 16]);
+                    if constexpr (C::SEPP) {
+                        // S_t is read: the next S_t may overwrite it.  P_t and O_t are
+                        // ours once the previous P_t V product is complete.
+                        tc_fence_before();
+                        mbar_arrive(bar(B_S_FREE + t));
+                        if (npv > 0) ok = __all_sync(0xffffffffu, wait(B_PV_DONE + t, (uint32_t)(npv - 1) & 1u));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_st16((C::SEPP ? p_tm : s_tm) + c * 16, &pk[c * 16]);
                     tmem_st_wait64(pk);
                     l_run = l_run * alpha + sum;
                     if (redo || (WIN && took_max && i > 0)) {
@@ -741,10 +921,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(bar(B_P_FULL + t));
+                if constexpr (C::SEPP) {
+                    if (i == 0 && pend) {
+                        // the previous item's O_t is complete (its last P_t V is): read it
+                        // out before this P_t is handed over, whose product overwrites O_t
+                        uint32_t o[D / 32][32];
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, o[c]);
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+                        tc_fence_before();
+                        mbar_arrive(bar(B_P_FULL + t));
+                        store_row(o, pm, pl, prow, pbh);
+                        pend = false;
+                    } else {
+                        tc_fence_before();
+                        mbar_arrive(bar(B_P_FULL + t));
+                    }
+                    ++npv;
+                } else {
+                    tc_fence_before();
+                    mbar_arrive(bar(B_P_FULL + t));
+                }
             }
             if (!ok) break;
+            if constexpr (C::SEPP) {  // epilogue deferred to the next item's first tile
+                pend = true;
+                pm = m_used;
+                pl = l_run;
+                prow = row_g;
+                pbh = g.bh;
+                continue;
+            }
             ok = __all_sync(0xffffffffu, wait(B_O_DONE + t, (uint32_t)od & 1u));
             ++od;
             if (!ok) break;
@@ -762,24 +970,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
             tc_fence_before();
             mbar_arrive(bar(B_O_FREE + t));
-            if (row_g < p.Sq) {
-                // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
-                const float inv_l = (F8 ? p.o_scale : 1.f) / l_run;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
-                                                       ((size_t)g.bh * p.Sq + row_g) * D);
+            store_row(o, m_used, l_run, row_g, g.bh);
+        }
+        if constexpr (C::SEPP) {
+            if (ok && pend) {  // the last item's epilogue
+                ok = __all_sync(0xffffffffu, wait(B_PV_DONE + t, (uint32_t)(npv - 1) & 1u));
+                if (ok) {
+                    tc_fence_after();
+                    uint32_t o[D / 32][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, o[c]);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {  // 16-byte unit (8 columns) c * 4 + u of the row
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(o[c][u * 8 + 2 * e]) * inv_l,
-                                               __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
-                        dst[c * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                p.lse[(size_t)g.bh * p.Sq + row_g] =
-                    (m_used - (F8 ? kF8PShift : 0.f) + lg2_approx(l_run)) * 0.69314718055994531f;
+                    for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+                    store_row(o, pm, pl, prow, pbh);
+                }
             }
         }
         if constexpr (tma_epilogue) {
