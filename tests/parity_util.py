@@ -3,8 +3,9 @@ ABI on seeded inputs and compare with the fp64 oracle.
 
 Tolerances (stated for this attention forward on bf16 inputs): max |dO| <= 2e-2,
 mean |dO| <= 2e-3, max |dLSE| <= 1e-3.  They cover bf16 rounding of P before
-P*V (relative 2^-9 per term), fp32 accumulation, the bf16 rounding of O
-(half an ulp is 2^-9 relative; 1.6e-2 absolute at |O| in [4, 8)) and
+P*V (at most 2^-8 relative per term: bf16 keeps 8 significant bits), fp32
+accumulation, the bf16 rounding of O (half an ulp is at most 2^-8 relative;
+1.6e-2 absolute at |O| in [4, 8)) and
 ex2.approx / lg2.approx (relative error ~2^-22).
 """
 import numpy as np
