@@ -575,8 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             return true;
                         };
                         if constexpr (!PERSIST) ok = q_ready(0) && (!g.act1 || q_ready(1));
+                        bool kready = false;  // K_FULL of key tile `it` already waited for
                         for (int it = 0; ok && it < N; ++it) {
-                            ok = wait(B_K_FULL + sk, kph);
+                            if (!kready) ok = wait(B_K_FULL + sk, kph);
+                            kready = false;
                             if (!ok) break;
                             tc_fence_after();
                             const bool p0 = it >= first0 && it <= last0;
@@ -616,6 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                             tc_commit(bar(B_K_EMPTY + sk));
+                            // the next key tile's K is waited for here, so that P0 V and
+                            // the next S0 issue back to back (S0 then waits on nothing)
+                            if (it + 1 < N) {
+                                ok = wait(B_K_FULL + (sk + 1 == C::KST ? 0 : sk + 1), sk + 1 == C::KST ? kph ^ 1u : kph);
+                                if (!ok) break;
+                                kready = true;
+                            }
                             if (p0) {
                                 ok = issue_pv(0, ipv0++, sv, vph);
                                 if (!ok) break;
@@ -711,11 +720,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                // S_t in two halves: the second half's load is in flight while the
+                // exp pass works on the first (a tile that needs the whole row
+                // first -- max, mask, 8-bit -- waits for both halves here)
                 uint32_t s[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                tmem_ld32(s_tm, s[0]);
+                tmem_ld32(s_tm + 32, s[1]);
+                tmem_ld_wait2(s[0], s[1]);
+                tmem_ld32(s_tm + 64, s[2]);
+                tmem_ld32(s_tm + 96, s[3]);
                 // A tile needs the mask unless every row of the sub-tile may see all
                 // of its keys (causal: only the diagonal tile; ragged: the last).
                 const int col0 = (my_jhi - i) * C::BN;
@@ -723,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            (p.wl >= 0 && col0 < r_last - p.wl))
                                         : (i == 0 && (p.wr >= 0 || (p.Sk % C::BN) != 0));
                 const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
+                if (F8 || masked || (WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : i == 0))
+                    tmem_ld_wait2(s[2], s[3]);
                 auto apply_mask = [&]() {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -853,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
+                            if (c == 2) tmem_ld_wait2(s[2], s[3]);  // the second half of S_t
                             if (use_skip && skip[c]) {
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) pk[c * 16 + e] = 0u;
