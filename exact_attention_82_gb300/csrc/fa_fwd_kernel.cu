@@ -144,9 +144,11 @@ enum : uint32_t {
     B_DRAIN = 32,
     B_S_FREE = 33,   // + sub-tile (separate P): the softmax warps have read S_t (128 arrivals)
     B_PV_DONE = 35,  // + sub-tile (separate P): a P_t V product is complete
+    B_P_HALF = 37,   // + sub-tile: the first half of P_t (keys 0-63) is written (128 arrivals)
+    B_PH_DONE = 39,  // + sub-tile: the P V product of that first half is complete
 };
-constexpr uint32_t SLOT_TMEM = 320;   // byte offset of the TMEM base address
-constexpr uint32_t SLOT_ABORT = 324;  // byte offset of the abort flag
+constexpr uint32_t SLOT_TMEM = 368;   // byte offset of the TMEM base address
+constexpr uint32_t SLOT_ABORT = 372;  // byte offset of the abort flag
 constexpr unsigned long long kDrainNs = 20ull * 1000 * 1000;  // 20 ms
 constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+2 idle)
 // Register split.  At launch every thread has 168 (3 warps per SM sub-partition);
@@ -268,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(B_S_FREE + t), 128);
             mbar_init(bar(B_PV_DONE + t), 1);
+            mbar_init(bar(B_P_HALF + t), 128);
+            mbar_init(bar(B_PH_DONE + t), 1);
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -423,11 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_ss(s_tm, dq + off, dks + off, C::IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            // O_t += P_t V (the item's first product overwrites O_t); its waits are the caller's
-            auto issue_pv_mma = [&](int t, bool accumulate, int stage) {
+            // O_t += P_t V over K-steps [k0, k1) (the item's first product
+            // overwrites O_t); its waits are the caller's
+            auto issue_pv_mma = [&](int t, bool accumulate, int stage, int k0, int k1) {
                 const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                    if (kk < k0 || kk >= k1) continue;
                     // A = P_t in TMEM (8 columns = 32 bytes of keys per step); B = V, MN-major
                     const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
                     if constexpr (F8)
@@ -562,15 +568,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
                         int svp = 0;          // V stage of the previous tile
                         uint32_t vpph = 0;
+                        // 16-bit inputs: P_t V in two halves, keys 0-63 once the softmax
+                        // has written them (P_HALF; their completion is committed to
+                        // PH_DONE), then keys 64-127 (P_FULL).  8-bit: in one piece.
                         auto issue_pv = [&](int t, int ipv, int stage, uint32_t phase) -> bool {
                             int &npv = t ? npv1 : npv0;
-                            if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                            if (!wait(F8 ? B_P_FULL + t : B_P_HALF + t, (uint32_t)npv & 1u)) return false;
                             if (!wait(B_V_FULL + stage, phase)) return false;
                             if constexpr (PERSIST) {
                                 if (ipv == 0 && !o_free(t)) return false;
                             }
                             tc_fence_after();
-                            issue_pv_mma(t, ipv > 0, stage);
+                            if constexpr (F8) {
+                                issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS);
+                            } else {
+                                issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS / 2);
+                                tc_commit(bar(B_PH_DONE + t));
+                                if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                                tc_fence_after();
+                                issue_pv_mma(t, true, stage, C::PV_STEPS / 2, C::PV_STEPS);
+                            }
                             ++npv;
                             return true;
                         };
@@ -769,6 +786,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 };
                 if (masked) mask_tile();
+                // O_t (this thread's row) times f, 16 columns at a time (few registers:
+                // it runs while part of S and P is held).  O_t is stable from "S_t
+                // full" until this sub-tile hands P_t (or its first half) over: S_t is
+                // issued after the previous P_t V.
+                auto scale_o = [&](float f) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t o[16];
+                        tmem_ld16(o_tm + c * 16, o);
+                        tmem_ld_wait16(o);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st16(o_tm + c * 16, o);
+                        tmem_st_wait16(o);
+                    }
+                };
+                // 16-bit inputs without separate P hand P_t to the MMA warp in two
+                // halves (keys 0-63, then 64-127): the first half's P V runs while
+                // the second half is computed.
+                auto hand_over_first_half = [&]() {
+                    tc_fence_before();
+                    mbar_arrive(bar(B_P_HALF + t));
+                };
                 if constexpr (F8) {
                     // The tile's row max every tile; the running max moves only when
                     // it is exceeded by more than kF8Lazy, and O is then rescaled.
@@ -795,8 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t nm2 = f2_pack(nm, nm);
                     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
                     uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    auto exp8 = [&](int c) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             float x0, x1, x2, x3;
@@ -813,13 +852,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[(2 * e + 1) & 3] = f2_add(acc[(2 * e + 1) & 3], f2_pack(p2, p3));
                             pk[c * 8 + e] = pack_e4m3x4(p0, p1, p2, p3);
                         }
+                    };
+                    // (P goes over in one piece: handing it over in halves measured
+                    // 2-4% slower for the 8-bit kernel)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) exp8(c);
+                    tmem_st32(s_tm, pk);
+                    tmem_st_wait(pk);
                     float a0, a1, b0, b1;
                     f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
                     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-                    tmem_st32(s_tm, pk);
-                    tmem_st_wait(pk);
                     l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
                     if (i > 0 && __any_sync(0xffffffffu, move)) {
+                        // O rescaled 32 columns at a time (S and P are no longer held here,
+                        // and the 8-bit max moves often enough for the width to matter)
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
@@ -833,12 +879,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     // P is computed against the max already in use.  The row max is
-                    // only taken on the first tile, or again for a tile whose sum shows
-                    // a score more than 2^64 above that max (the sum also catches inf
-                    // and NaN): then the tile is redone against its true max.  S is
-                    // still intact in TMEM then, because P is stored after the check.
+                    // only taken on the first tile, or again when a score shows up
+                    // more than 2^64 above that max (the sum of a half tile shows it,
+                    // and inf and NaN too).  In the first half (nothing handed over
+                    // yet, S intact in TMEM) the tile is redone against its true max;
+                    // in the second half the max is raised to that half's and, once the
+                    // first half's product has reached O, O is rescaled.
                     const uint64_t c2 = f2_pack(sl2, sl2);
-                    float alpha = 1.f, sum = 0.f;
+                    float alpha = 1.f;
                     uint32_t pk[64];
                     auto take_max = [&]() {
                         // row max: four independent chains of three-input max
@@ -858,16 +906,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         alpha = (WIN && m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
                         m_used = m_new;
                     };
-                    // use_skip: honour skipped chunks (a masked tile of full or causal
-                    // attention); every other tile takes the straight-line pass
-                    auto exp_pass = [&](bool use_skip) {
-                        // p = 2^(s*scale*log2e - m): packed FMA pairs, then MUFU ex2;
-                        // row sum in four packed partial sums
+                    // p = 2^(s*scale*log2e - m) for chunks [cb, ce): packed FMA pairs,
+                    // then MUFU ex2; the sum in four packed partial sums.  use_skip:
+                    // honour skipped chunks (a masked tile of full or causal attention
+                    // with separate P); every other tile takes the straight-line pass.
+                    auto exp_range = [&](int cb, int ce, bool use_skip) -> float {
                         const float nm = (WIN && m_used == -INFINITY) ? 0.f : -m_used;  // all-masked row: p = 0
                         const uint64_t nm2 = f2_pack(nm, nm);
                         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
+                            if (c < cb || c >= ce) continue;
                             if (c == 2) tmem_ld_wait2(s[2], s[3]);  // the second half of S_t
                             if (use_skip && skip[c]) {
 #pragma unroll
@@ -889,28 +938,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float a0, a1, b0, b1;
                         f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
                         f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-                        sum = (a0 + a1) + (b0 + b1);
+                        return (a0 + a1) + (b0 + b1);
                     };
-                    // the max is taken while any row of the warp has no allowed key
-                    // yet (always on the first tile)
-                    const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
-                    const bool skips = C::SEPP && !WIN && masked;
-                    if (took_max) take_max();
-                    if (skips)
-                        exp_pass(true);
-                    else
-                        exp_pass(false);
-                    const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
-                    if (redo) {
+                    auto reload_s = [&]() {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s[c]);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-                        if (masked) mask_tile();
-                        take_max();
-                        exp_pass(false);  // a redo is never on a masked tile of full or causal attention
-                    }
+                    };
+                    // the max is taken while any row of the warp has no allowed key
+                    // yet (always on the first tile)
+                    const bool took_max = WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : (i == 0);
+                    if (took_max) take_max();
                     if constexpr (C::SEPP) {
+                        const bool skips = !WIN && masked;
+                        float sum = skips ? exp_range(0, 4, true) : exp_range(0, 4, false);
+                        const bool redo = !took_max && __any_sync(0xffffffffu, !(sum <= 0x1p64f));
+                        if (redo) {
+                            reload_s();
+                            if (masked) mask_tile();
+                            take_max();
+                            sum = exp_range(0, 4, false);  // a redo is never on a masked tile of full or causal attention
+                        }
                         // S_t is read: the next S_t may overwrite it.  P_t and O_t are
                         // ours once the previous P_t V product is complete.
                         tc_fence_before();
@@ -918,23 +967,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (npv > 0) ok = __all_sync(0xffffffffu, wait(B_PV_DONE + t, (uint32_t)(npv - 1) & 1u));
                         if (!ok) break;
                         tc_fence_after();
-                    }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_st16((C::SEPP ? p_tm : s_tm) + c * 16, &pk[c * 16]);
-                    tmem_st_wait64(pk);
-                    l_run = l_run * alpha + sum;
-                    if (redo || (WIN && took_max && i > 0)) {
-                        // O holds the earlier tiles relative to the old max: rescale it
-    #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32(o_tm + c * 32, o);
-                            tmem_ld_wait(o);
-    #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(o_tm + c * 32, o);
-                            tmem_st_wait(o);
+                        for (int c = 0; c < 4; ++c) tmem_st16(p_tm + c * 16, &pk[c * 16]);
+                        tmem_st_wait64(pk);
+                        l_run = l_run * alpha + sum;
+                        if (redo || (WIN && took_max && i > 0)) scale_o(alpha);
+                    } else {
+                        float sa = exp_range(0, 2, false);
+                        const bool redo = !took_max && __any_sync(0xffffffffu, !(sa <= 0x1p64f));
+                        if (redo) {
+                            reload_s();
+                            if (masked) mask_tile();
+                            take_max();
+                            sa = exp_range(0, 2, false);
                         }
+                        if (redo || (WIN && took_max && i > 0)) scale_o(alpha);  // O holds earlier tiles at the old max
+                        tmem_st16(s_tm, pk);  // keys 0-63: columns 0-31
+                        tmem_st16(s_tm + 16, pk + 16);
+                        tmem_st_wait(*reinterpret_cast<const uint32_t(*)[32]>(pk));
+                        hand_over_first_half();
+                        float sb = exp_range(2, 4, false);
+                        float beta = 1.f;
+                        if (!took_max && !redo && __any_sync(0xffffffffu, !(sb <= 0x1p64f))) {
+                            // the first half's product must be in O before O is rescaled
+                            ok = __all_sync(0xffffffffu, wait(B_PH_DONE + t, (uint32_t)(ns - 1) & 1u));
+                            if (!ok) break;
+                            tc_fence_after();
+                            // keys 64-127 of S_t are still in TMEM (only columns 0-31 hold P)
+                            tmem_ld32(s_tm + 64, s[2]);
+                            tmem_ld32(s_tm + 96, s[3]);
+                            tmem_ld_wait2(s[2], s[3]);
+                            if (masked) mask_tile();
+                            float mq[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                            for (int c = 2; c < 4; ++c)
+#pragma unroll
+                                for (int e = 0; e < 32; e += 4)
+#pragma unroll
+                                    for (int q = 0; q < 2; ++q)
+                                        mq[q] = max3f(mq[q], __uint_as_float(s[c][e + 2 * q]),
+                                                      __uint_as_float(s[c][e + 2 * q + 1]));
+                            const float m_new = fmaxf(m_used, fmaxf(mq[0], mq[1]) * sl2);
+                            beta = ex2_approx(m_used - m_new);
+                            m_used = m_new;
+                            scale_o(beta);
+                            sb = exp_range(2, 4, false);
+                        }
+                        tmem_st16(s_tm + 32, pk + 32);  // keys 64-127: columns 32-63
+                        tmem_st16(s_tm + 48, pk + 48);
+                        tmem_st_wait(*reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                        l_run = (l_run * alpha + sa) * beta + sb;
                     }
                 }
                 if constexpr (C::SEPP) {

@@ -187,16 +187,17 @@ def test_forward_kernel_gives_up_cleanly(D):
     assert fa.fa_device_status() == fa.FA_OK
 
 
-def _growing_scores(D, lift, causal):
-    """Keys of the first key tile (index 0, processed last) score `lift` (in
-    exp2 units) above every other key, so later tiles outgrow the max taken
-    from the first tile processed."""
+def _growing_scores(D, lift, causal, keys=(0, 128)):
+    """Keys [keys[0], keys[1]) of the first key tile (index 0, processed last)
+    score `lift` (in exp2 units) above every other key, so later tiles outgrow
+    the max taken from the first tile processed."""
     B, H, S = 1, 2, 384
     q, k, v = make_qkv(B, H, S, S, D, seed=21)
     q = torch.ones_like(q)  # every score is (scale) * sum(k_j)
     target = lift * (D ** 0.5) / 1.4426950408889634 / D  # per-element key value
     k = k * 0.05
-    k[:, :, :128] = (k[:, :, :128].float() + target).to(torch.bfloat16)
+    a, b = keys
+    k[:, :, a:b] = (k[:, :, a:b].float() + target).to(torch.bfloat16)
     return q, k, v
 
 
@@ -210,6 +211,21 @@ def test_scores_growing_past_first_tile_max(D, lift, causal):
     og, lg = run_gpu(q, k, v, D ** -0.5, causal)
     ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), D ** -0.5, causal)
     compare(og, lg, *ref, f"lift {lift} D{D}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("keys", [(0, 64), (64, 128), (60, 70)], ids=["first-half", "second-half", "both-halves"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scores_growing_in_part_of_a_tile(D, keys, causal):
+    """Scores more than 2^64 past the max in use in only part of a key tile.
+    The 16-bit D = 128 kernel hands P over in two halves (keys 0-63, 64-127):
+    an overflow in the first half redoes the tile before anything is handed
+    over; one only in the second half raises the max after the first half's
+    product has reached O, rescales O and redoes the second half."""
+    q, k, v = _growing_scores(D, 70.0, causal, keys)
+    og, lg = run_gpu(q, k, v, D ** -0.5, causal)
+    ref = oracle.attn_fwd(*(bf16_bits(t) for t in (q, k, v)), D ** -0.5, causal)
+    compare(og, lg, *ref, f"keys {keys} D{D}")
 
 
 # ------------------------------------------------- many items per launch
