@@ -146,9 +146,9 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
     const long long BH = (long long)B * H;
     const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
     if (!encode_bhsd(&tm_q, q, D, Sq, BH, fa::kBlockM) || !encode_bhsd(&tm_k, k, D, Sk, BH, fa::kBlockN) ||
-        !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
+        !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN))
         return fail_cuda(cudaErrorInvalidValue);
     fa::FwdParams p;
     p.o = o;
@@ -165,7 +165,7 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.o_scale = 1.f;
     p.timeout_ns = timeout_ns;
-    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, tm_o, p, sm_count(), (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
 }
@@ -214,9 +214,9 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
         overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, o, o_bytes))
         return FA_ERR_ALIAS;
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v;
     if (!encode_bhsd(&tm_q, q, D, Sq, BH, fa::kBlockM, 1) || !encode_bhsd(&tm_k, k, D, Sk, BH, fa::kBlockN, 1) ||
-        !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN, 1) || !encode_bhsd(&tm_o, o, D, Sq, BH, fa::kBlockM))
+        !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN, 1))
         return fail_cuda(cudaErrorInvalidValue);
     fa::FwdParams p;
     p.o = o;
@@ -233,7 +233,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale_log2;
     p.o_scale = descale_v;
     p.timeout_ns = kWaitLimitNs;
-    const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, tm_o, p, sm_count(), (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
 }

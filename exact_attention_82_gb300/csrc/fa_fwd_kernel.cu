@@ -8,10 +8,9 @@
 //
 // Mapping onto the chip.  The work items are the (query block, batch x head)
 // pairs of the same page's launch grid (section "第一处源码差异：launch grid
-// 怎么铺"); for full and causal attention the kernel is persistent: one CTA
-// per SM takes one item per round of gridDim.x items, in snake order (causal:
-// all heads' longest query blocks first; a bounded band runs one CTA per
-// item).  TMEM is allocated and the barriers initialised once, and the next
+// 怎么铺"); the kernel is persistent: one CTA per SM takes one item per round
+// of gridDim.x items, in snake order (causal: all heads' longest query blocks
+// first).  TMEM is allocated and the barriers initialised once, and the next
 // item's Q and first K/V tiles load while the current item finishes, which
 // takes the fixed cost of a CTA (launch, setup, load latency, epilogue) off
 // every item but the first.  Each item is 256 query rows as two 128-row
@@ -30,14 +29,14 @@
 //                O0 += P0_j V_j
 //              so that while the tensor core works on one sub-tile the other
 //              sub-tile's softmax runs (each softmax has two MMAs of slack);
+//              16-bit D = 128 takes P_t V in two halves of 64 keys, the first
+//              as soon as the softmax has written it;
 //   warps 0-3  softmax of sub-tile 0, warps 4-7 of sub-tile 1: thread r owns
 //              query row r (TMEM lane r): it reads its S row from TMEM, masks
 //              (only on its first key tile), updates the running max and sum,
 //              writes P (bf16) back over its S row in TMEM, where the P V MMA
-//              reads it as its A operand, and at the end scales O by 1/l,
-//              writes its O row (a persistent CTA to global memory directly;
-//              a CTA with one item through shared memory and a TMA store)
-//              and LSE.
+//              reads it as its A operand, and at the end scales O by 1/l and
+//              writes its O row straight to global memory, and its LSE.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
 // the first 64 columns of S_t (128 bf16 packed in pairs) -- except at 16-bit
 // D = 64, where the 128 columns O leaves free hold P0 and P1 on their own
@@ -160,11 +159,8 @@ static_assert(256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register spli
 
 // Query buffers: two per sub-tile where they fit in shared memory (D = 64 and
 // the 8-bit path), so that a persistent CTA loads the next item's Q while the
-// current item runs; a three-tile ring for persistent 16-bit D = 128 (see
-// FwdCfg); one per sub-tile for one item per CTA.
-__host__ __device__ constexpr int query_buffers(int D, bool F8, bool PERSIST) {
-    return (PERSIST && (D == 64 || F8)) ? 2 : (PERSIST ? 3 : 1);
-}
+// current item runs; a three-tile ring for 16-bit D = 128 (see FwdCfg).
+__host__ __device__ constexpr int query_buffers(int D, bool F8) { return (D == 64 || F8) ? 2 : 3; }
 
 // One work item: 256 query rows (two sub-tiles) of one (batch, head), and the
 // key tiles [jlo_t, jhi_t] each sub-tile needs.  Key tiles are loaded from J
@@ -220,15 +216,11 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
 // (full or causal attention) only a sub-tile's first key tile can need a mask
 // and every row has an allowed key in it, which the code below exploits.
 // F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
-// PERSIST: the grid may be smaller than the item count, so a CTA walks items
-// and hands Q and O buffers over between them; without it every CTA has one
-// item and the hand-over code is compiled out of the MMA-issue loop.
-template <int D, bool WIN, bool F8, bool PERSIST>
+template <int D, bool WIN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdParams p) {
-    constexpr int QB = query_buffers(D, F8, PERSIST);
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    constexpr int QB = query_buffers(D, F8);
     using C = FwdCfg<D, F8, QB>;
     static_assert(!(F8 && WIN), "the 8-bit path has no bounded band");
     extern __shared__ uint8_t smem_raw[];
@@ -575,9 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             int &npv = t ? npv1 : npv0;
                             if (!wait(F8 ? B_P_FULL + t : B_P_HALF + t, (uint32_t)npv & 1u)) return false;
                             if (!wait(B_V_FULL + stage, phase)) return false;
-                            if constexpr (PERSIST) {
-                                if (ipv == 0 && !o_free(t)) return false;
-                            }
+                            if (ipv == 0 && !o_free(t)) return false;
                             tc_fence_after();
                             if constexpr (F8) {
                                 issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS);
@@ -591,7 +581,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ++npv;
                             return true;
                         };
-                        if constexpr (!PERSIST) ok = q_ready(0) && (!g.act1 || q_ready(1));
                         bool kready = false;  // K_FULL of key tile `it` already waited for
                         for (int it = 0; ok && it < N; ++it) {
                             if (!kready) ok = wait(B_K_FULL + sk, kph);
@@ -601,18 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const bool p0 = it >= first0 && it <= last0;
                             const bool p1 = it >= first1 && it <= last1;
                             if (p0) {
-                                if constexpr (PERSIST) {
-                                    if (it == first0) {
-                                        ok = q_ready(0);
-                                        if (!ok) break;
-                                        tc_fence_after();
-                                    }
+                                if (it == first0) {
+                                    ok = q_ready(0);
+                                    if (!ok) break;
+                                    tc_fence_after();
                                 }
                                 issue_s(dq0, tmem, sk);
                                 tc_commit(bar(B_S_FULL + 0));
-                                if constexpr (PERSIST) {
-                                    if (it == last0) tc_commit(bar(qf0));
-                                }
+                                if (it == last0) tc_commit(bar(qf0));
                             }
                             if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
                                 ok = issue_pv(1, ipv1++, svp, vpph);
@@ -621,18 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_commit(bar(B_V_EMPTY + svp));
                             }
                             if (p1) {
-                                if constexpr (PERSIST) {
-                                    if (it == first1) {
-                                        ok = q_ready(1);
-                                        if (!ok) break;
-                                        tc_fence_after();
-                                    }
+                                if (it == first1) {
+                                    ok = q_ready(1);
+                                    if (!ok) break;
+                                    tc_fence_after();
                                 }
                                 issue_s(dq1, tmem + 128, sk);
                                 tc_commit(bar(B_S_FULL + 1));
-                                if constexpr (PERSIST) {
-                                    if (it == last1) tc_commit(bar(qf1));
-                                }
+                                if (it == last1) tc_commit(bar(qf1));
                             }
                             tc_commit(bar(B_K_EMPTY + sk));
                             // the next key tile's K is waited for here, so that P0 V and
@@ -709,13 +690,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             p.lse[(size_t)bh * p.Sq + rg] = (m - (F8 ? kF8PShift : 0.f) + lg2_approx(l)) * 0.69314718055994531f;
         };
-        // With one item per CTA (not PERSIST) and 16-bit inputs, O is staged in
-        // this sub-tile's Q buffer, free once the item's MMAs are done, and
-        // written by a TMA store after the loop; a persistent CTA stores each
-        // row directly, so that its Q buffer can take the next item's Q as
-        // early as possible.
-        constexpr bool tma_epilogue = !F8 && !PERSIST;
-        bool ok = true, staged = false;
+        // Each thread stores its own O row straight from registers, so a sub-tile's
+        // Q buffer can take the next item's Q as early as possible.
+        bool ok = true;
         Item g;
         float m_used = -INFINITY;  // max in exp2 units (raw score * scale*log2e) used for P
         float l_run = 0.f;         // sum of P over the keys seen, relative to m_used
@@ -1054,10 +1031,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait(B_O_DONE + t, (uint32_t)od & 1u));
             ++od;
             if (!ok) break;
-            if constexpr (tma_epilogue) {  // the only item of this CTA: epilogue below
-                staged = true;
-                break;
-            }
             // ---- epilogue: O_t out of TMEM (after which the next item may
             // overwrite it), O / l -> bf16 -> this row of O in global memory; LSE
             tc_fence_after();
@@ -1083,47 +1056,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_row(o, pm, pl, prow, pbh);
                 }
             }
-        }
-        if constexpr (tma_epilogue) {
-            // ---- O / l -> bf16 -> shared memory (this sub-tile's Q buffer) ->
-            // TMA store; LSE.  Both named barriers run whatever `ok` says, so
-            // no warp can be left waiting.
-            named_bar_sync(1 + t, 128);
-            const uint32_t sO = sQ + t * C::QT_BYTES;
-            const int row_g = g.row0 + t * C::BM + row;
-            if (staged && ok) {
-                tc_fence_after();
-                const float inv_l = 1.f / l_run;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(o_tm + c * 32, o);
-                    tmem_ld_wait(o);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int U = c * 4 + u;  // 16-byte unit (8 columns) of the row
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv_l,
-                                               __uint_as_float(o[u * 8 + 2 * e + 1]) * inv_l);
-                        const uint32_t addr = sO + (U >> 3) * C::CHUNK + row * 128 +
-                                              ((((uint32_t)U & 7u) ^ ((uint32_t)row & 7u)) << 4);
-                        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-                    }
-                }
-                fence_proxy_async_smem();
-            }
-            named_bar_sync(1 + t, 128);
-            if (staged && ok && row == 0 && *abort_flag == 0u) {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_store_3d(&tm_o, sO + c * C::CHUNK, c * 64, g.row0 + t * C::BM, g.bh);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-            }
-            if (staged && ok && row_g < p.Sq)
-                p.lse[(size_t)g.bh * p.Sq + row_g] = (m_used + lg2_approx(l_run)) * 0.69314718055994531f;
         }
     }
 
@@ -1153,41 +1085,34 @@ __global__ void fa_wait_selftest(unsigned long long limit_ns) {
     __syncthreads();
 }
 
-template <int D, bool WIN, bool F8, bool PERSIST>
+template <int D, bool WIN, bool F8>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                const CUtensorMap &tm_o, const FwdParams &p, int n_ctas, cudaStream_t stream) {
-    constexpr uint32_t smem = FwdCfg<D, F8, query_buffers(D, F8, PERSIST)>::SMEM;
+                                const FwdParams &p, int num_sms, cudaStream_t stream) {
+    constexpr uint32_t smem = FwdCfg<D, F8, query_buffers(D, F8)>::SMEM;
     cudaError_t e =
-        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8, PERSIST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fa_fwd_sm103a<D, WIN, F8, PERSIST><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, tm_o, p);
+    // Persistent CTAs (at most one per SM, each walking many items) take the
+    // fixed cost of a CTA off every item but the first and even out items of
+    // different length (causal: longest first, dealt out in snake order).
+    const int n_ctas = p.n_items > num_sms ? num_sms : p.n_items;
+    fa_fwd_sm103a<D, WIN, F8><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, p);
     return cudaGetLastError();
 }
 
-// Persistent CTAs (one per SM, each walking many items) take the fixed cost
-// of a CTA off every item but the first and even out items of different
-// length (causal: longest first, dealt out in snake order); for the bounded
-// bands of D = 128, one CTA per item with its TMA-store epilogue measured
-// faster.
-static int grid_for(const FwdParams &p, bool persistent, int num_sms) {
-    return (persistent && p.n_items > num_sms) ? num_sms : p.n_items;
-}
-
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream) {
+                       const FwdParams &p, int num_sms, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
-    const bool persistent = D == 64 || !win;
-    const int n_ctas = grid_for(p, persistent, num_sms);
     if (D == 64)
-        return win ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream)
-                   : launch_fwd_d<64, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    if (win) return launch_fwd_d<128, true, false, false>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
-    return launch_fwd_d<128, false, false, true>(tm_q, tm_k, tm_v, tm_o, p, n_ctas, stream);
+        return win ? launch_fwd_d<64, true, false>(tm_q, tm_k, tm_v, p, num_sms, stream)
+                   : launch_fwd_d<64, false, false>(tm_q, tm_k, tm_v, p, num_sms, stream);
+    return win ? launch_fwd_d<128, true, false>(tm_q, tm_k, tm_v, p, num_sms, stream)
+               : launch_fwd_d<128, false, false>(tm_q, tm_k, tm_v, p, num_sms, stream);
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream) {
-    return launch_fwd_d<128, false, true, true>(tm_q, tm_k, tm_v, tm_o, p, grid_for(p, true, num_sms), stream);
+                           const FwdParams &p, int num_sms, cudaStream_t stream) {
+    return launch_fwd_d<128, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream);
 }
 
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream) {

@@ -70,14 +70,13 @@ cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, cons
 cudaError_t bwd_status_read_and_clear(int *out);
 
 // Launch the forward kernel for head dim D (64 or 128) over the p.n_items
-// work items: persistent CTAs (at most num_sms) or one CTA per item, chosen
-// by the kind of attention; tm_o is the TMA map of O for the latter.
+// work items on persistent CTAs (at most num_sms).
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream);
+                       const FwdParams &p, int num_sms, cudaStream_t stream);
 
 // Launch the 8-bit (e4m3 Q, K, V; D = 128; full or causal) forward kernel.
 cudaError_t launch_fwd_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_o, const FwdParams &p, int num_sms, cudaStream_t stream);
+                           const FwdParams &p, int num_sms, cudaStream_t stream);
 
 // Device status word: read it (after synchronising `stream`) and reset it.
 cudaError_t status_read_and_clear(int *out, cudaStream_t stream);
