@@ -40,9 +40,11 @@
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_t sits in
 // the first 64 columns of S_t (128 bf16 packed in pairs) -- except at 16-bit
 // D = 64, where the 128 columns O leaves free hold P0 and P1 on their own
-// [384,448) [448,512): the next S_t is then issued as soon as the softmax has
-// read S_t, instead of after P_t V has consumed P_t, and an item's O epilogue
-// is deferred to the next item's first tile (see SEPP below).
+// [384,448) [448,512), and in the 8-bit path, where P_t (128 one-byte keys a
+// row) goes to a shared-memory tile that the P V MMA reads as its A operand.
+// With P separate the next S_t is issued as soon as the softmax has read S_t,
+// instead of after P_t V has consumed P_t, and an item's O epilogue is
+// deferred to the next item's first tile (see SEPP below).
 //
 // The row max is taken on a sub-tile's first key tile only (16-bit path);
 // later tiles compute P against that stale max, which is exact because O and
@@ -96,16 +98,22 @@ struct FwdCfg {
     static constexpr uint32_t OFF_Q = 0;                  // query tile slots
     static constexpr uint32_t OFF_K = OFF_Q + NQ * QT_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
+    // separate P (below): the 8-bit path keeps P_t in shared memory, 128 rows of
+    // 128 one-byte keys (K-major, 128-byte swizzle), the A operand of its P V MMA
+    static constexpr bool P_SMEM = F8;
+    static constexpr uint32_t P_BYTES = P_SMEM ? BM * BN * EB : 0;  // one sub-tile's P
+    static constexpr uint32_t OFF_P = OFF_V + VST * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr uint32_t BAR_BYTES = 384;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256;
-    // 16-bit D = 64 leaves 128 TMEM columns free: P_t gets its own 64 there
-    // instead of overwriting S_t, so the next S_t can be issued as soon as
-    // the softmax has read S_t (not only after P_t V has consumed P_t)
-    static constexpr bool SEPP = D == 64 && !F8;
-    static constexpr uint32_t TM_P = TM_O + 2 * D;  // SEPP: P_t at TM_P + 64 t
+    // Separate P: P_t does not overwrite S_t, so the next S_t can be issued as
+    // soon as the softmax has read S_t (not only after P_t V has consumed P_t).
+    // 16-bit D = 64 puts P_t in the 128 TMEM columns O leaves free; the 8-bit
+    // path in shared memory (P_SMEM).
+    static constexpr bool SEPP = D == 64 || F8;
+    static constexpr uint32_t TM_P = TM_O + 2 * D;  // 16-bit separate P: P_t at TM_P + 64 t
     // one MMA takes 32 bytes of the contraction: 16 bf16 or 32 e4m3 elements
     static constexpr int S_STEPS = D * EB / 32;
     static constexpr int PV_STEPS = BN * EB / 32;
@@ -115,7 +123,7 @@ struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(!F8 || D == 128, "8-bit rows must fill one 128-byte swizzle atom");
     static_assert(BM == 128 && BN == 128, "tile");
-    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_BAR % 1024 == 0, "atoms");
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(SMEM > 114 * 1024, "one CTA per SM (it takes all TMEM columns)");
 };
@@ -401,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dqb = sw128_desc(sQ, 16, 1024);  // query buffer 0 of sub-tile 0
             const uint64_t dk = sw128_desc(sK, 16, 1024);
             const uint64_t dv = sw128_desc(sV, C::CHUNK, 1024);
+            const uint64_t dp = sw128_desc(sbase + C::OFF_P, 16, 1024);  // 8-bit P_0 (shared memory)
             int sk = 0, sv = 0;       // ring stage of the next K and V tile to be read, over all items
             uint32_t kph = 0, vph = 0;
             int qn0 = 0, qn1 = 0;     // items so far in which sub-tile 0 / 1 took part
@@ -427,13 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                     if (kk < k0 || kk >= k1) continue;
                     // A = P_t in TMEM (8 columns = 32 bytes of keys per step); B = V, MN-major
-                    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-                    if constexpr (F8)
-                        tc_mma_ts_f8(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
-                                     C::IDESC_PV, acc);
-                    else
-                        tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
-                                  C::IDESC_PV, acc);
+                    tc_mma_ts(tmem + C::TM_O + t * D, tmem + t * 128 + kk * 8, dvs + ((kk * C::V_STEP) >> 4),
+                              C::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
             // before an item's first S_t: its Q_t has landed
@@ -444,13 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return q == 0 || wait(B_O_FREE + t, (uint32_t)(q - 1) & 1u);
             };
             if constexpr (C::SEPP) {
-                // P in its own TMEM columns (16-bit D = 64).  Per key tile: S0_j and
-                // S1_j, each as soon as the softmax has read the previous S_t
-                // (S_FREE), then the P V products of the previous key tile -- so
-                // that, across an item boundary too, the next S runs while this
-                // item's last softmax is still computing.  (Issuing each sub-tile's
-                // S and previous P V together, S0 PV0 S1 PV1, measured slower.)
-                // Each P_t V product
+                // Separate P (own TMEM columns at 16-bit D = 64, shared memory at
+                // 8 bits).  Per key tile: S0_j and S1_j, each as soon as the softmax
+                // has read the previous S_t (S_FREE), then the P V products of the
+                // previous key tile -- so that, across an item boundary too, the next
+                // S runs while this item's last softmax is still computing.  (Issuing
+                // each sub-tile's S and previous P V together, S0 PV0 S1 PV1,
+                // measured slower.)  Each P_t V product
                 // commits PV_DONE_t, after which the softmax may overwrite P_t,
                 // rescale O_t or (after an item's last product) read O_t out.  The
                 // softmax reads an item's O_t before it signals the next item's
@@ -470,10 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait(B_V_FULL + stage, phase)) return false;
                     tc_fence_after();
                     const uint64_t dvs = dv + ((stage * C::KV_BYTES) >> 4);
+                    if constexpr (C::P_SMEM) {
+                        const uint64_t dps = dp + ((t * C::P_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < C::PV_STEPS; ++kk)
-                        tc_mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_P + t * 64 + kk * 8,
-                                  dvs + ((kk * C::V_STEP) >> 4), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                            tc_mma_ss_f8(tmem + C::TM_O + t * D, dps + ((kk * 32) >> 4), dvs + ((kk * C::V_STEP) >> 4),
+                                         C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                            tc_mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_P + t * 64 + kk * 8,
+                                      dvs + ((kk * C::V_STEP) >> 4), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit(bar(B_PV_DONE + t));
                     ++npv;
                     return true;
@@ -560,24 +572,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Tile by tile: S0_j, PV1_{j-1}, S1_j, PV0_j.
                         int svp = 0;          // V stage of the previous tile
                         uint32_t vpph = 0;
-                        // 16-bit inputs: P_t V in two halves, keys 0-63 once the softmax
-                        // has written them (P_HALF; their completion is committed to
-                        // PH_DONE), then keys 64-127 (P_FULL).  8-bit: in one piece.
+                        // P_t V in two halves: keys 0-63 once the softmax has written them
+                        // (P_HALF; their completion is committed to PH_DONE), then keys
+                        // 64-127 (P_FULL)
                         auto issue_pv = [&](int t, int ipv, int stage, uint32_t phase) -> bool {
                             int &npv = t ? npv1 : npv0;
-                            if (!wait(F8 ? B_P_FULL + t : B_P_HALF + t, (uint32_t)npv & 1u)) return false;
+                            if (!wait(B_P_HALF + t, (uint32_t)npv & 1u)) return false;
                             if (!wait(B_V_FULL + stage, phase)) return false;
                             if (ipv == 0 && !o_free(t)) return false;
                             tc_fence_after();
-                            if constexpr (F8) {
-                                issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS);
-                            } else {
-                                issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS / 2);
-                                tc_commit(bar(B_PH_DONE + t));
-                                if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
-                                tc_fence_after();
-                                issue_pv_mma(t, true, stage, C::PV_STEPS / 2, C::PV_STEPS);
-                            }
+                            issue_pv_mma(t, ipv > 0, stage, 0, C::PV_STEPS / 2);
+                            tc_commit(bar(B_PH_DONE + t));
+                            if (!wait(B_P_FULL + t, (uint32_t)npv & 1u)) return false;
+                            tc_fence_after();
+                            issue_pv_mma(t, true, stage, C::PV_STEPS / 2, C::PV_STEPS);
                             ++npv;
                             return true;
                         };
@@ -659,7 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + t * 128;
         const uint32_t o_tm = tmem + lane_off + C::TM_O + t * D;
-        const uint32_t p_tm = tmem + lane_off + C::TM_P + t * 64;  // separate P only
+        const uint32_t p_tm = tmem + lane_off + C::TM_P + t * 64;  // 16-bit separate P only
+        const uint32_t p_sm = sbase + C::OFF_P + t * C::P_BYTES + row * 128;  // 8-bit: this thread's P row
+        const uint32_t p_sw = (uint32_t)row & 7u;  // 128-byte swizzle of that row
         const float sl2 = p.scale_log2;
         int ns = 0;  // S_t tiles so far, over all items (S_FULL phases)
         int od = 0;  // items so far in which this sub-tile took part (O_DONE phases)
@@ -732,6 +742,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
                 if (F8 || masked || (WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : i == 0))
                     tmem_ld_wait2(s[2], s[3]);
+                if constexpr (C::P_SMEM) {
+                    // the 8-bit path redoes nothing (its max is taken every tile), so
+                    // S_t may be overwritten as soon as it is in registers
+                    tc_fence_before();
+                    mbar_arrive(bar(B_S_FREE + t));
+                }
                 auto apply_mask = [&]() {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -830,16 +846,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[c * 8 + e] = pack_e4m3x4(p0, p1, p2, p3);
                         }
                     };
-                    // (P goes over in one piece: handing it over in halves measured
-                    // 2-4% slower for the 8-bit kernel)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) exp8(c);
-                    tmem_st32(s_tm, pk);
-                    tmem_st_wait(pk);
                     float a0, a1, b0, b1;
                     f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
                     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
                     l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
+                    // P_t's buffer and O_t are ours once the previous P_t V product is complete
+                    if (npv > 0) ok = __all_sync(0xffffffffu, wait(B_PV_DONE + t, (uint32_t)(npv - 1) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                    // this row of P_t: eight 16-byte units, swizzled as the MMA reads them
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(p_sm + (((uint32_t)u ^ p_sw) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                                     pk[4 * u + 3]);
+                    fence_proxy_async_smem();  // visible to the tensor core before P_FULL
                     if (i > 0 && __any_sync(0xffffffffu, move)) {
                         // O rescaled 32 columns at a time (S and P are no longer held here,
                         // and the 8-bit max moves often enough for the width to matter)
