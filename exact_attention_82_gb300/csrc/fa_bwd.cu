@@ -50,6 +50,14 @@ struct BwdCfg {
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * T * 4;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;  // S, dP, accumulator(s)
+    // dQ kernel: key tiles are taken in halves of 64 keys whose S and dP alternate
+    // between two TMEM buffers (S: [64 b, 64 b + 64), dP: [128 + 64 b, ...)), so the
+    // next half's MMAs run while the element-wise warps work on this one; Q and dO
+    // also sit in TMEM (bf16 pairs, row = lane) as the A operands of S = Q K^T and
+    // dP = dO V^T, which then read only K and V from shared memory
+    static constexpr uint32_t TM_Q = TM_ACC + D, TM_DO = TM_Q + D / 2;
+    static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(T, T / 2, false);  // M=T, N=T/2, K-major
+    static_assert(TM_DO + D / 2 <= 512, "TMEM columns");
     static constexpr uint32_t IDESC_SS = idesc_bf16_f32(T, T, false);  // M=T, N=T, both K-major
     static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(T, D, true);  // M=T, N=D, B MN-major
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -63,6 +71,8 @@ enum : uint32_t {
     BB_DONE = 6,       // last accumulation finished
     BB_DRAIN = 7,
     BB_CH_FULL = 8,    // + chunk (4): 32 columns of element-wise results in TMEM (128 arrivals)
+    BB_QT = 12,        // dQ kernel: Q and dO copied into TMEM (128 arrivals)
+    BB_X_FULL2 = 13,   // dQ kernel: S and dP of a half tile computed in TMEM buffer 1
 };
 constexpr uint32_t BSLOT_TMEM = 128, BSLOT_ABORT = 132;
 constexpr unsigned long long kBwdDrainNs = 20ull * 1000 * 1000;
@@ -102,6 +112,8 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < 4; ++c) mbar_init(bar(BB_CH_FULL + c), 128);
         mbar_init(bar(BB_DONE), 1);
         mbar_init(bar(BB_DRAIN), 1);
+        mbar_init(bar(BB_QT), 128);
+        mbar_init(bar(BB_X_FULL2), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -149,41 +161,53 @@ __global__ void __launch_bounds__(192, 1)
                 return __all_sync(0xffffffffu,
                                   mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT));
             };
-            const uint64_t da = sw128_desc(sbase + C::OFF_A, 16, 1024);   // Q, K-major
-            const uint64_t db = sw128_desc(sbase + C::OFF_B, 16, 1024);   // dO, K-major
             const uint64_t dk1 = sw128_desc(sbase + C::OFF_R1, 16, 1024);         // K as B of S (K-major)
             const uint64_t dk2 = sw128_desc(sbase + C::OFF_R1, C::CHUNK, 1024);   // K as B of dQ (MN-major)
             const uint64_t dv1 = sw128_desc(sbase + C::OFF_R2, 16, 1024);         // V as B of dP (K-major)
-            bool ok = wait(BB_RES, 0);
-            for (int it = 0; ok && it < N; ++it) {
-                const int st = it & 1;
-                ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t so = (st * C::TILE) >> 4;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-                    tc_mma_ss(tmem + C::TM_X, da + off, dk1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
-                    tc_mma_ss(tmem + C::TM_Y, db + off, dv1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(BB_X_FULL));
-                // dQ += dS K chunk by chunk, each 32-key chunk as soon as the
-                // element-wise warps have written it (A = dS in TMEM, B = K MN-major)
-                for (int c = 0; ok && c < 4; ++c) {
-                    ok = wait(BB_CH_FULL + c, (uint32_t)it & 1u);
-                    if (!ok) break;
+            bool ok = wait(BB_QT, 0);  // Q and dO are in TMEM
+            // dQ += dS K for half g (two 32-key chunks, each as soon as the element-wise
+            // warps have written it; A = dS in TMEM buffer g mod 2, B = K MN-major)
+            auto issue_dq = [&](int g) -> bool {
+                const int bb = g & 1;
+                const uint32_t so = ((uint32_t)((g >> 1) & 1) * C::TILE) >> 4;
+                for (int c = 0; c < 2; ++c) {
+                    if (!wait(BB_CH_FULL + 2 * bb + c, (uint32_t)(g >> 1) & 1u)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int kk = 2 * c + h;
-                        tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + kk * 8, dk2 + so + ((kk * 2048) >> 4),
-                                  C::IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
+                        const int kk = 2 * c + h;  // 16-key step within the half
+                        tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + 64 * bb + kk * 8,
+                                  dk2 + so + (((uint32_t)(64 * bb + 16 * kk) * 128) >> 4), C::IDESC_ACC,
+                                  (g > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                if (!ok) break;
-                tc_commit(bar(BB_EMPTY + st));
+                if (bb == 1) tc_commit(bar(BB_EMPTY + ((g >> 1) & 1)));  // both halves of the tile are read
+                return true;
+            };
+            for (int g = 0; ok && g < 2 * N; ++g) {
+                const int it = g >> 1, bb = g & 1, st = it & 1;
+                if (bb == 0) {
+                    ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // S and dP of keys [64 bb, 64 bb + 64) of tile `it` into buffer bb: the
+                // buffer's previous half was read by the element-wise warps (its chunks
+                // were waited for) and its dQ MMAs were issued before these
+                const uint32_t so = (st * C::TILE) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // A = Q or dO in TMEM (8 columns = 16 elements per step); B = K or V rows
+                    const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32 + bb * 64 * 128) >> 4;
+                    tc_mma_ts(tmem + C::TM_X + 64 * bb, tmem + C::TM_Q + kk * 8, dk1 + so + off, C::IDESC_HALF,
+                              kk > 0 ? 1u : 0u);
+                    tc_mma_ts(tmem + C::TM_Y + 64 * bb, tmem + C::TM_DO + kk * 8, dv1 + so + off, C::IDESC_HALF,
+                              kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(bb ? BB_X_FULL2 : BB_X_FULL));
+                if (g > 0) ok = issue_dq(g - 1);
             }
+            if (ok) ok = issue_dq(2 * N - 1);
             if (ok) tc_commit(bar(BB_DONE));
             tc_commit(bar(BB_DRAIN));
             mbar_wait_drain(bar(BB_DRAIN), 0, kBwdDrainNs);
@@ -196,6 +220,29 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const uint32_t x_tm = tmem + lane_off + C::TM_X, y_tm = tmem + lane_off + C::TM_Y;
         const uint32_t acc_tm = tmem + lane_off + C::TM_ACC;
+        // this row of Q and of dO from the shared-memory tiles (128-byte swizzle) into
+        // TMEM, where the MMA warp takes them as A operands
+        bool ok = wait(BB_RES, 0);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t src = sbase + (m ? C::OFF_B : C::OFF_A) + row * 128;
+                const uint32_t dst = tmem + lane_off + (m ? C::TM_DO : C::TM_Q);
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        ld_shared_v4(src + c * C::CHUNK + (((uint32_t)u ^ ((uint32_t)row & 7u)) << 4), v[4 * u],
+                                     v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    tmem_st32(dst + c * 32, v);
+                    tmem_st_wait(v);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(BB_QT));
+        }
         // Delta_i = dO_i . O_i (also stored for the dK/dV kernel); lse in exp2 units
         float delta = 0.f, lse2 = INFINITY;
         if (valid_row) {
@@ -222,22 +269,22 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
         const uint64_t nl2 = f2_pack(-lse2, -lse2);
         const uint64_t nd2 = f2_pack(-delta, -delta);
-        bool ok = true;
-        for (int it = 0; it < N; ++it) {
-            if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
+        for (int g = 0; g < 2 * N; ++g) {  // 64-key halves, buffer g mod 2
+            const int bb = g & 1;
+            if (ok) ok = wait(bb ? BB_X_FULL2 : BB_X_FULL, (uint32_t)(g >> 1) & 1u);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int col0 = (j_hi - it) * C::T;
+            const int col0 = (j_hi - (g >> 1)) * C::T + 64 * bb;
             const int lim = (p.causal ? min(p.Sk, row_g + 1) : p.Sk) - col0;
             // keys at or past `lim` are out (only the first tile: causal diagonal, ragged end)
             auto chunks = [&](bool masked) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t pk[16];
                     uint32_t s[32], dp[32];
-                    tmem_ld32(x_tm + c * 32, s);
-                    tmem_ld32(y_tm + c * 32, dp);
+                    tmem_ld32(x_tm + 64 * bb + c * 32, s);
+                    tmem_ld32(y_tm + 64 * bb + c * 32, dp);
                     tmem_ld_wait(s);
                     tmem_ld_wait(dp);
 #pragma unroll
@@ -256,13 +303,14 @@ __global__ void __launch_bounds__(192, 1)
                                   d0, d1);
                         pk[e] = b16_pack(d0, d1);
                     }
-                    tmem_st16(x_tm + c * 16, pk);
+                    // dS (bf16) over columns of this half's S already read
+                    tmem_st16(x_tm + 64 * bb + c * 16, pk);
                     tmem_st_wait16(pk);
                     tc_fence_before();
-                    mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
+                    mbar_arrive(bar(BB_CH_FULL + 2 * bb + c));  // the MMA warp may take this chunk
                 }
             };
-            if (it == 0 && mask_first)
+            if ((g >> 1) == 0 && mask_first)
                 chunks(true);
             else
                 chunks(false);
@@ -340,6 +388,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(BB_EMPTY + s), 1);
         }
         mbar_init(bar(BB_X_FULL), 1);
+        mbar_init(bar(BB_X_FULL2), 1);
         for (int c = 0; c < 4; ++c) mbar_init(bar(BB_CH_FULL + c), 128);
         mbar_init(bar(BB_DONE), 1);
         mbar_init(bar(BB_DRAIN), 1);
@@ -357,6 +406,9 @@ __global__ void __launch_bounds__(192, 1)
     auto wait = [&](uint32_t b, uint32_t parity) {
         return mbar_wait(bar(b), parity, abort_flag, p.timeout_ns, &g_status_bwd, FA_ERR_TIMEOUT);
     };
+    // As in the dQ kernel, query tiles are taken in halves of 64 queries whose S^T
+    // and dP^T alternate between two TMEM buffers ([64 b, 64 b + 64) and
+    // [128 + 64 b, ...)); the two accumulators take the remaining 2 D columns.
     const uint32_t TM_DV = C::TM_ACC, TM_DK = C::TM_ACC + D;
 
     if (warp == 4) {
@@ -398,37 +450,47 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t do1 = sw128_desc(sbase + C::OFF_R2, 16, 1024);         // dO as B of dP^T
             const uint64_t do2 = sw128_desc(sbase + C::OFF_R2, C::CHUNK, 1024);   // dO as B of dV (MN-major)
             bool ok = wait(BB_RES, 0);
-            for (int it = 0; ok && it < N; ++it) {
-                const int st = it & 1;
-                ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
-                if (!ok) break;
-                tc_fence_after();
+            // dV += P^T dO (A = P^T over S^T) and dK += dS^T Q (A = dS^T over dP^T) for
+            // half g, each 32-query chunk as soon as the element-wise warps have written it
+            auto issue_acc = [&](int g) -> bool {
+                const int bb = g & 1;
+                const uint32_t so = ((uint32_t)((g >> 1) & 1) * C::TILE) >> 4;
+                for (int c = 0; c < 2; ++c) {
+                    if (!wait(BB_CH_FULL + 2 * bb + c, (uint32_t)(g >> 1) & 1u)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * c + h;  // 16-query step within the half
+                        const uint32_t boff = ((uint32_t)(64 * bb + 16 * kk) * 128) >> 4;
+                        const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+                        tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + 64 * bb + kk * 8, do2 + so + boff, C::IDESC_ACC, acc);
+                        tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + 64 * bb + kk * 8, dq2 + so + boff, C::IDESC_ACC, acc);
+                    }
+                }
+                if (bb == 1) tc_commit(bar(BB_EMPTY + ((g >> 1) & 1)));  // both halves of the tile are read
+                return true;
+            };
+            for (int g = 0; ok && g < 2 * N; ++g) {
+                const int it = g >> 1, bb = g & 1, st = it & 1;
+                if (bb == 0) {
+                    ok = wait(BB_FULL + st, (uint32_t)(it >> 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // S^T and dP^T of queries [64 bb, 64 bb + 64) of tile `it` into buffer bb
+                // (that buffer's previous half has been read and its MMAs issued)
                 const uint32_t so = (st * C::TILE) >> 4;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-                    tc_mma_ss(tmem + C::TM_X, dka + off, dq1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
-                    tc_mma_ss(tmem + C::TM_Y, dva + off, do1 + so + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+                    const uint32_t boff = off + ((uint32_t)(bb * 64 * 128) >> 4);
+                    tc_mma_ss(tmem + C::TM_X + 64 * bb, dka + off, dq1 + so + boff, C::IDESC_HALF, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + C::TM_Y + 64 * bb, dva + off, do1 + so + boff, C::IDESC_HALF, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(BB_X_FULL));
-                // dV += P^T dO (A = P^T over S^T) and dK += dS^T Q (A = dS^T over dP^T),
-                // each 32-query chunk as soon as the element-wise warps have written it
-                for (int c = 0; ok && c < 4; ++c) {
-                    ok = wait(BB_CH_FULL + c, (uint32_t)it & 1u);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kk = 2 * c + h;
-                        tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + kk * 8, do2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
-                        tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + kk * 8, dq2 + so + ((kk * 2048) >> 4), C::IDESC_ACC,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                if (!ok) break;
-                tc_commit(bar(BB_EMPTY + st));
+                tc_commit(bar(bb ? BB_X_FULL2 : BB_X_FULL));
+                if (g > 0) ok = issue_acc(g - 1);
             }
+            if (ok) ok = issue_acc(2 * N - 1);
             if (ok) tc_commit(bar(BB_DONE));
             tc_commit(bar(BB_DRAIN));
             mbar_wait_drain(bar(BB_DRAIN), 0, kBwdDrainNs);
@@ -441,34 +503,36 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t x_tm = tmem + lane_off + C::TM_X, y_tm = tmem + lane_off + C::TM_Y;
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
         bool ok = true;
-        for (int it = 0; it < N; ++it) {
-            // this tile's query rows, negated for the packed arithmetic below: -lse
-            // (exp2 units; -inf past Sq, so P = 0) and -Delta
+        for (int g = 0; g < 2 * N; ++g) {  // 64-query halves, buffer g mod 2
+            const int it = g >> 1, bb = g & 1;
             const int qt = i_lo + it;
             float *lv = vec + (it & 1) * 256;
-            {
+            if (bb == 0) {
+                // this tile's query rows, negated for the packed arithmetic below: -lse
+                // (exp2 units; -inf past Sq, so P = 0) and -Delta
                 const int qg = qt * C::T + row;
                 const size_t r = (size_t)bh * p.Sq + qg;
                 lv[row] = qg < p.Sq ? -(p.lse[r] * 1.4426950408889634f) : -INFINITY;
                 lv[128 + row] = qg < p.Sq ? -p.delta[r] : 0.f;
+                named_bar_sync(1, 128);
             }
-            named_bar_sync(1, 128);
-            if (ok) ok = wait(BB_X_FULL, (uint32_t)it & 1u);
+            if (ok) ok = wait(bb ? BB_X_FULL2 : BB_X_FULL, (uint32_t)(g >> 1) & 1u);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
                 // columns (queries) in pairs: (-lse, -Delta) of queries cc, cc+1 as
                 // one 64-bit shared load each; P^T and dS^T two columns per instruction
-                const uint64_t *nl = reinterpret_cast<const uint64_t *>(lv);
-                const uint64_t *nd = reinterpret_cast<const uint64_t *>(lv + 128);
-                const int lim = key_g - qt * C::T;  // diagonal tile: query cc sees this key iff cc >= lim
+                const uint64_t *nl = reinterpret_cast<const uint64_t *>(lv) + 32 * bb;
+                const uint64_t *nd = reinterpret_cast<const uint64_t *>(lv + 128) + 32 * bb;
+                // diagonal tile: query cc (of this half) sees this key iff cc >= lim
+                const int lim = key_g - qt * C::T - 64 * bb;
                 auto chunks = [&](bool masked) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t pk[16], dk[16];
                         uint32_t s[32], dp[32];
-                        tmem_ld32(x_tm + c * 32, s);
-                        tmem_ld32(y_tm + c * 32, dp);
+                        tmem_ld32(x_tm + 64 * bb + c * 32, s);
+                        tmem_ld32(y_tm + 64 * bb + c * 32, dp);
                         tmem_ld_wait(s);
                         tmem_ld_wait(dp);
 #pragma unroll
@@ -490,12 +554,13 @@ __global__ void __launch_bounds__(192, 1)
                             pk[e] = b16_pack(p0, p1);
                             dk[e] = b16_pack(d0, d1);
                         }
-                        tmem_st16(x_tm + c * 16, pk);
-                        tmem_st16(y_tm + c * 16, dk);
+                        // P^T and dS^T (bf16) over columns of this half already read
+                        tmem_st16(x_tm + 64 * bb + c * 16, pk);
+                        tmem_st16(y_tm + 64 * bb + c * 16, dk);
                         tmem_st_wait16(pk);
                         tmem_st_wait16(dk);
                         tc_fence_before();
-                        mbar_arrive(bar(BB_CH_FULL + c));  // the MMA warp may take this chunk
+                        mbar_arrive(bar(BB_CH_FULL + 2 * bb + c));  // the MMA warp may take this chunk
                     }
                 };
                 if (it == 0 && mask_first)  // diagonal: keys above the query are out
