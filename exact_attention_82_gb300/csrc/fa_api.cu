@@ -375,15 +375,14 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
             if (overlaps(outs[a], out_b[a], outs[b], out_b[b])) return FA_ERR_ALIAS;
     }
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
-    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, to, tdq, tdk, tdv;
     if (!encode_bhsd(&tq, q, D, Sq, BH, 128) || !encode_bhsd(&tk, k, D, Sk, BH, 128) ||
         !encode_bhsd(&tv, v, D, Sk, BH, 128) || !encode_bhsd(&tdo, dout, D, Sq, BH, 128) ||
+        !encode_bhsd(&to, o, D, Sq, BH, 128) ||
         !encode_bhsd(&tdq, dq, D, Sq, BH, 128) || !encode_bhsd(&tdk, dk, D, Sk, BH, 128) ||
         !encode_bhsd(&tdv, dv, D, Sk, BH, 128))
         return fail_cuda(cudaErrorInvalidValue);
     fa::BwdParams p;
-    p.o = o;
-    p.dout = dout;
     p.lse = lse;
     p.delta = delta;
     p.Sq = Sq;
@@ -394,7 +393,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = kWaitLimitNs;
-    const cudaError_t e = fa::launch_bwd(D, tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, (cudaStream_t)stream);
+    const cudaError_t e = fa::launch_bwd(D, tq, tk, tv, tdo, to, tdq, tdk, tdv, p, BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
 }

@@ -49,6 +49,10 @@ struct BwdCfg {
     static constexpr uint32_t OFF_VEC = 6 * TILE;      // [2 parity][2: -lse2, -delta][128] fp32
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * T * 4;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    // dQ kernel: the O tile (for Delta) where the dK/dV kernel keeps its vectors
+    static constexpr uint32_t OFF_O = OFF_VEC;
+    static constexpr uint32_t OFF_BAR_DQ = OFF_O + TILE;
+    static constexpr uint32_t SMEM_DQ = OFF_BAR_DQ + 256 + 1024;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;  // S, dP, accumulator(s)
     // dQ kernel: key tiles are taken in halves of 64 keys whose S and dP alternate
     // between two TMEM buffers (S: [64 b, 64 b + 64), dP: [128 + 64 b, ...)), so the
@@ -60,7 +64,7 @@ struct BwdCfg {
     static_assert(TM_DO + D / 2 <= 512, "TMEM columns");
     static constexpr uint32_t IDESC_SS = idesc_bf16_f32(T, T, false);  // M=T, N=T, both K-major
     static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(T, D, true);  // M=T, N=D, B MN-major
-    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(SMEM <= 227 * 1024 && SMEM_DQ <= 227 * 1024, "shared memory");
 };
 
 enum : uint32_t {
@@ -84,7 +88,8 @@ template <int D>
 __global__ void __launch_bounds__(192, 1)
     fa_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
+              const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -98,10 +103,10 @@ __global__ void __launch_bounds__(192, 1)
     const int j_hi = p.causal ? min(n_kt - 1, mt) : n_kt - 1;
     const int N = j_hi + 1;
     const bool mask_first = p.causal || (p.Sk % C::T) != 0;
-    const uint32_t bars = sbase + C::OFF_BAR;
+    const uint32_t bars = sbase + C::OFF_BAR_DQ;
     auto bar = [&](uint32_t i) { return bars + 8u * i; };
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_ABORT);
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR + BSLOT_TMEM);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR_DQ + BSLOT_ABORT);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::OFF_BAR_DQ + BSLOT_TMEM);
     if (threadIdx.x == 0) {
         mbar_init(bar(BB_RES), 1);
         for (int s = 0; s < 2; ++s) {
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
         fence_mbar_init();
     }
     if (warp == 5) {
-        tmem_alloc(sbase + C::OFF_BAR + BSLOT_TMEM, 512);
+        tmem_alloc(sbase + C::OFF_BAR_DQ + BSLOT_TMEM, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -132,10 +137,11 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 4) {
         if (lane == 0) {  // ---- TMA producer: Q, dO once; K_j, V_j per tile (j descending)
             const uint64_t pol = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(BB_RES), 2 * C::TILE);
+            mbar_arrive_expect_tx(bar(BB_RES), 3 * C::TILE);
             for (int c = 0; c < C::NCH; ++c) {
                 tma_load_3d(sbase + C::OFF_A + c * C::CHUNK, &tm_q, c * 64, mt * C::T, bh, bar(BB_RES), pol);
                 tma_load_3d(sbase + C::OFF_B + c * C::CHUNK, &tm_do, c * 64, mt * C::T, bh, bar(BB_RES), pol);
+                tma_load_3d(sbase + C::OFF_O + c * C::CHUNK, &tm_o, c * 64, mt * C::T, bh, bar(BB_RES), pol);
             }
             int issued = 0;
             for (int it = 0; it < N; ++it) {
@@ -243,17 +249,18 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_before();
             mbar_arrive(bar(BB_QT));
         }
-        // Delta_i = dO_i . O_i (also stored for the dK/dV kernel); lse in exp2 units
+        // Delta_i = dO_i . O_i (also stored for the dK/dV kernel) from the O and dO
+        // tiles in shared memory, 16-byte units in row order; lse in exp2 units
         float delta = 0.f, lse2 = INFINITY;
-        if (valid_row) {
+        if (ok && valid_row) {
             const size_t r = (size_t)bh * p.Sq + row_g;
-            const uint4 *og = reinterpret_cast<const uint4 *>(p.o) + r * (D / 8);
-            const uint4 *dg = reinterpret_cast<const uint4 *>(p.dout) + r * (D / 8);
             float acc = 0.f;
 #pragma unroll 4
             for (int u = 0; u < D / 8; ++u) {
-                const uint4 a = og[u], b = dg[u];
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+                const uint32_t at = (uint32_t)(u >> 3) * C::CHUNK + row * 128 + ((((uint32_t)u & 7u) ^ ((uint32_t)row & 7u)) << 4);
+                uint32_t aw[4], bw[4];
+                ld_shared_v4(sbase + C::OFF_O + at, aw[0], aw[1], aw[2], aw[3]);
+                ld_shared_v4(sbase + C::OFF_B + at, bw[0], bw[1], bw[2], bw[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
@@ -618,17 +625,19 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-int bwd_smem_bytes(int D) { return D == 64 ? (int)BwdCfg<64>::SMEM : (int)BwdCfg<128>::SMEM; }
+int bwd_smem_bytes(int D) {
+    return D == 64 ? (int)max(BwdCfg<64>::SMEM, BwdCfg<64>::SMEM_DQ) : (int)max(BwdCfg<128>::SMEM, BwdCfg<128>::SMEM_DQ);
+}
 
 template <int D>
 static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk,
+                                const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq, const CUtensorMap &tdk,
                                 const CUtensorMap &tdv, const BwdParams &p, long long BH, cudaStream_t stream) {
-    const int smem = (int)BwdCfg<D>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = (int)BwdCfg<D>::SMEM, smem_dq = (int)BwdCfg<D>::SMEM_DQ;
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_dq);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(fa_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fa_bwd_dq<D><<<dim3((unsigned)(p.n_qt * BH)), dim3(192), smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+    fa_bwd_dq<D><<<dim3((unsigned)(p.n_qt * BH)), dim3(192), smem_dq, stream>>>(tq, tk, tv, tdo, to, tdq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     fa_bwd_dkdv<D><<<dim3((unsigned)(p.n_kt * BH)), dim3(192), smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
@@ -636,10 +645,10 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, co
 }
 
 cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk, const CUtensorMap &tdv,
-                       const BwdParams &p, long long BH, cudaStream_t stream) {
-    if (D == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, stream);
-    return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, BH, stream);
+                       const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq, const CUtensorMap &tdk,
+                       const CUtensorMap &tdv, const BwdParams &p, long long BH, cudaStream_t stream) {
+    if (D == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, to, tdq, tdk, tdv, p, BH, stream);
+    return launch_bwd_d<128>(tq, tk, tv, tdo, to, tdq, tdk, tdv, p, BH, stream);
 }
 
 cudaError_t bwd_status_read_and_clear(int *out) {

@@ -53,8 +53,6 @@ cudaError_t splitkv_scratch(void **out);
 
 // Backward launch (dQ kernel, then dK/dV kernel).
 struct BwdParams {
-    const void *o;       // bf16 [B*H, Sq, D]  forward output
-    const void *dout;    // bf16 [B*H, Sq, D]  its gradient
     const float *lse;    // fp32 [B*H, Sq]     forward log-sum-exp (natural log)
     float *delta;        // fp32 [B*H, Sq]     workspace: rowsum(dO * O)
     int Sq, Sk;
@@ -65,8 +63,8 @@ struct BwdParams {
 };
 int bwd_smem_bytes(int D);
 cudaError_t launch_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &tdk, const CUtensorMap &tdv,
-                       const BwdParams &p, long long BH, cudaStream_t stream);
+                       const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq, const CUtensorMap &tdk,
+                       const CUtensorMap &tdv, const BwdParams &p, long long BH, cudaStream_t stream);
 cudaError_t bwd_status_read_and_clear(int *out);
 
 // Launch the forward kernel for head dim D (64 or 128) over the p.n_items
