@@ -176,17 +176,15 @@ __global__ void __launch_bounds__(192, 1)
             auto issue_dq = [&](int g) -> bool {
                 const int bb = g & 1;
                 const uint32_t so = ((uint32_t)((g >> 1) & 1) * C::TILE) >> 4;
-                for (int c = 0; c < 2; ++c) {
-                    if (!wait(BB_CH_FULL + 2 * bb + c, (uint32_t)(g >> 1) & 1u)) return false;
-                    tc_fence_after();
+                // both 32-key chunks of the half's dS (the element-wise warps signal the
+                // second, written after the first)
+                if (!wait(BB_CH_FULL + 2 * bb + 1, (uint32_t)(g >> 1) & 1u)) return false;
+                tc_fence_after();
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kk = 2 * c + h;  // 16-key step within the half
-                        tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + 64 * bb + kk * 8,
-                                  dk2 + so + (((uint32_t)(64 * bb + 16 * kk) * 128) >> 4), C::IDESC_ACC,
-                                  (g > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
+                for (int kk = 0; kk < 4; ++kk)  // 16-key steps within the half
+                    tc_mma_ts(tmem + C::TM_ACC, tmem + C::TM_X + 64 * bb + kk * 8,
+                              dk2 + so + (((uint32_t)(64 * bb + 16 * kk) * 128) >> 4), C::IDESC_ACC,
+                              (g > 0 || kk > 0) ? 1u : 0u);
                 if (bb == 1) tc_commit(bar(BB_EMPTY + ((g >> 1) & 1)));  // both halves of the tile are read
                 return true;
             };
@@ -313,8 +311,10 @@ __global__ void __launch_bounds__(192, 1)
                     // dS (bf16) over columns of this half's S already read
                     tmem_st16(x_tm + 64 * bb + c * 16, pk);
                     tmem_st_wait16(pk);
-                    tc_fence_before();
-                    mbar_arrive(bar(BB_CH_FULL + 2 * bb + c));  // the MMA warp may take this chunk
+                    if (c == 1) {  // the half's dS is written: the MMA warp may take it
+                        tc_fence_before();
+                        mbar_arrive(bar(BB_CH_FULL + 2 * bb + 1));
+                    }
                 }
             };
             if ((g >> 1) == 0 && mask_first)
@@ -462,17 +462,16 @@ __global__ void __launch_bounds__(192, 1)
             auto issue_acc = [&](int g) -> bool {
                 const int bb = g & 1;
                 const uint32_t so = ((uint32_t)((g >> 1) & 1) * C::TILE) >> 4;
-                for (int c = 0; c < 2; ++c) {
-                    if (!wait(BB_CH_FULL + 2 * bb + c, (uint32_t)(g >> 1) & 1u)) return false;
-                    tc_fence_after();
+                // both 32-query chunks of the half (the element-wise warps signal the
+                // second, written after the first)
+                if (!wait(BB_CH_FULL + 2 * bb + 1, (uint32_t)(g >> 1) & 1u)) return false;
+                tc_fence_after();
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kk = 2 * c + h;  // 16-query step within the half
-                        const uint32_t boff = ((uint32_t)(64 * bb + 16 * kk) * 128) >> 4;
-                        const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
-                        tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + 64 * bb + kk * 8, do2 + so + boff, C::IDESC_ACC, acc);
-                        tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + 64 * bb + kk * 8, dq2 + so + boff, C::IDESC_ACC, acc);
-                    }
+                for (int kk = 0; kk < 4; ++kk) {  // 16-query steps within the half
+                    const uint32_t boff = ((uint32_t)(64 * bb + 16 * kk) * 128) >> 4;
+                    const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_ts(tmem + TM_DV, tmem + C::TM_X + 64 * bb + kk * 8, do2 + so + boff, C::IDESC_ACC, acc);
+                    tc_mma_ts(tmem + TM_DK, tmem + C::TM_Y + 64 * bb + kk * 8, dq2 + so + boff, C::IDESC_ACC, acc);
                 }
                 if (bb == 1) tc_commit(bar(BB_EMPTY + ((g >> 1) & 1)));  // both halves of the tile are read
                 return true;
@@ -566,8 +565,10 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_st16(y_tm + 64 * bb + c * 16, dk);
                         tmem_st_wait16(pk);
                         tmem_st_wait16(dk);
-                        tc_fence_before();
-                        mbar_arrive(bar(BB_CH_FULL + 2 * bb + c));  // the MMA warp may take this chunk
+                        if (c == 1) {  // the half's P^T and dS^T are written: the MMA warp may take them
+                            tc_fence_before();
+                            mbar_arrive(bar(BB_CH_FULL + 2 * bb + 1));
+                        }
                     }
                 };
                 if (it == 0 && mask_first)  // diagonal: keys above the query are out
