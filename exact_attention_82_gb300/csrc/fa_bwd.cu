@@ -22,8 +22,11 @@
 // Both kernels: warps 0-3 element-wise (thread = TMEM lane = output row),
 // warp 4 TMA producer, warp 5 TMEM allocation and MMA issue (the whole warp
 // runs the issue loop, one elected lane issues each instruction).
-// Rows are handled in 32-column chunks; chunk c's bf16 result is written to
-// columns [16c, 16c+16), all of which the thread has already read.
+// Each 128-row tile of the loop is taken in two halves of 64 whose S and dP
+// (S^T and dP^T) alternate between two TMEM buffers, so the MMAs of the next
+// half run while the element-wise warps work on this one.  A half's rows are
+// handled in two 32-column chunks; chunk c's bf16 result is written to the
+// half's columns [16c, 16c+16), all of which the thread has already read.
 #include <math.h>
 #include <stdint.h>
 
