@@ -56,8 +56,9 @@
 // (exp2 units) past the max in use.  The 8-bit path takes the row max every
 // tile and moves the running max when it is exceeded by more than 2 (P must
 // fit e4m3).  O_t is stable while sub-tile t is between "S_t full" and
-// "P_t full" (S_t is issued after the previous P_t V), so the softmax thread
-// rescales its own O row there when needed.
+// "P_t full" (S_t is issued after the previous P_t V; with P separate, from
+// the previous P_t V's PV_DONE on), so the softmax thread rescales its own O
+// row there when needed.
 //
 // Key tiles run from the last one to the first, so the only tile of a
 // sub-tile that needs masking (causal diagonal or ragged last tile) is its
