@@ -76,11 +76,36 @@ def source_group(path: str) -> str:
     return path if path in ("bwd", "splitkv") else "fwd"
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character
+    literals are kept as they are), so that a comment edit leaves the key of
+    the kernel's DRAM record unchanged while any code change alters it."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(group: str = "fwd") -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[group]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_strip_comments(f.read()).encode("utf-8"))
     return h.hexdigest()
 
 

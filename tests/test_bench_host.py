@@ -87,6 +87,18 @@ def test_traffic_record_needs_current_sources(tmp_path, monkeypatch):
     assert bench.traffic_per_launch(w) is None
 
 
+def test_source_key_ignores_comments_but_not_code():
+    """The key of a DRAM record survives comment edits but not code edits."""
+    base = 'int f(int x) { return x + 1; }  // add one\nconst char *s = "// kept";\n'
+    same = '/* header */\nint f(int x) { return x + 1; }\n\nconst char *s = "// kept"; // note\n'
+    code = 'int f(int x) { return x + 2; }  // add one\nconst char *s = "// kept";\n'
+    lit = 'int f(int x) { return x + 1; }  // add one\nconst char *s = "// kapt";\n'
+    k = bench._strip_comments
+    assert k(base) == k(same)
+    assert k(base) != k(code) and k(base) != k(lit)
+    assert '"// kept"' in k(base)
+
+
 @pytest.mark.parametrize("causal,wl,r0,rows", [(True, 40, 50, 30), (True, -1, 10, 20), (False, -1, 64, 7),
                                                (True, 8, 0, 16)])
 def test_reference_sampler_rows_equal_full_computation(monkeypatch, causal, wl, r0, rows):
