@@ -15,7 +15,7 @@ import threading
 from . import build as _build
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_strerror", "fa_device_status",
-           "fa_selftest_bounded_wait", "fa_selftest_fwd_timeout", "fa_version", "FAError", "lib", "library_path",
+           "fa_selftest_bounded_wait", "fa_selftest_fwd_timeout", "fa_selftest_bwd_timeout", "fa_version", "FAError", "lib", "library_path",
            "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
@@ -62,6 +62,8 @@ _SIGNATURES = {
     "fa_selftest_bounded_wait": (_i, [_i, _vp]),
     "fa_selftest_fwd_timeout": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float,
                                      _i, ctypes.c_ulonglong, _vp]),
+    "fa_selftest_bwd_timeout": (_i, [_vp] * 10 + [_i, _i, _i, _i, _i, ctypes.c_float, _i, ctypes.c_ulonglong,
+                                                  _vp]),
     "fa_version": (_i, []),
 }
 
@@ -318,4 +320,17 @@ def fa_selftest_fwd_timeout(q, k, v, o, lse, scale, causal, timeout_ns: int, str
     Sk = k.shape[2]
     return lib().fa_selftest_fwd_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          lse.data_ptr(), B, H, Sq, Sk, D, float(scale),
+                                         int(bool(causal)), int(timeout_ns), _stream_ptr(stream))
+
+
+def fa_selftest_bwd_timeout(q, k, v, o, lse, dout, dq, dk, dv, delta, scale, causal, timeout_ns: int,
+                            stream=None) -> int:
+    """fa_bwd with every on-chip wait of both kernels bounded by `timeout_ns`
+    (tests of the give-up path); returns the launch status.  All arguments are
+    contiguous CUDA tensors as for fa_bwd."""
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    return lib().fa_selftest_bwd_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                         dv.data_ptr(), delta.data_ptr(), B, H, Sq, Sk, D, float(scale),
                                          int(bool(causal)), int(timeout_ns), _stream_ptr(stream))

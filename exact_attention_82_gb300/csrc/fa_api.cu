@@ -347,9 +347,9 @@ extern "C" int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *
 }
 
 // ------------------------------------------------------------------ backward
-extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                      const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H, int Sq, int Sk,
-                      int D, float scale, int causal, void *stream) {
+static int bwd_checked(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                       const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H, int Sq, int Sk,
+                       int D, float scale, int causal, void *stream, unsigned long long timeout_ns) {
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta) return FA_ERR_NULLPTR;
     const void *ptrs[10] = {q, k, v, o, lse, dout, dq, dk, dv, delta};
     for (const void *ptr : ptrs)
@@ -392,10 +392,25 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     p.causal = causal;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.timeout_ns = kWaitLimitNs;
+    p.timeout_ns = timeout_ns;
     const cudaError_t e = fa::launch_bwd(D, tq, tk, tv, tdo, to, tdq, tdk, tdv, p, BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
+}
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H, int Sq, int Sk,
+                      int D, float scale, int causal, void *stream) {
+    return bwd_checked(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Sq, Sk, D, scale, causal, stream,
+                       kWaitLimitNs);
+}
+
+extern "C" int fa_selftest_bwd_timeout(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                                       const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H,
+                                       int Sq, int Sk, int D, float scale, int causal, unsigned long long timeout_ns,
+                                       void *stream) {
+    if (timeout_ns > kWaitLimitNs) return FA_ERR_BAD_SHAPE;
+    return bwd_checked(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Sq, Sk, D, scale, causal, stream, timeout_ns);
 }
 
 extern "C" int fa_device_status(void *stream) {

@@ -268,6 +268,23 @@ int fa_selftest_fwd_timeout(const void *q, const void *k, const void *v, void *o
                             int B, int H, int Sq, int Sk, int D, float scale, int causal,
                             unsigned long long timeout_ns, void *stream);
 
+/*
+ * fa_selftest_bwd_timeout -- fa_bwd with every on-chip wait of both backward
+ * kernels bounded by `timeout_ns` (0 .. 2e9) instead of the 2 s that fa_bwd
+ * uses.  With a limit shorter than a tile load the kernels' own give-up path
+ * runs, as for fa_selftest_fwd_timeout: the CTA's abort flag is raised and
+ * FA_ERR_TIMEOUT recorded in the status word, the other roles stop at their
+ * next wait, copies and MMAs in flight are waited for (bounded), TMEM is freed
+ * and the CTA returns.  dQ, dK, dV and delta are then undefined.  Arguments,
+ * checks and errors are fa_bwd's, plus FA_ERR_BAD_SHAPE for timeout_ns above
+ * 2e9.  The surveyed pages have no counterpart: it exists so tests can show
+ * the backward kernels wind down cleanly and leave the context usable.
+ */
+int fa_selftest_bwd_timeout(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                            const void *dout, void *dq, void *dk, void *dv, float *delta, int B, int H,
+                            int Sq, int Sk, int D, float scale, int causal, unsigned long long timeout_ns,
+                            void *stream);
+
 /* fa_version -- library version, major*10000 + minor*100 + patch. */
 int fa_version(void);
 

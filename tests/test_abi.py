@@ -177,6 +177,13 @@ def test_bwd_argument_checks():
     assert bcall(ptrs=P[:6] + [P[0] + 16] + P[7:]) == fa.FA_ERR_ALIAS   # dq over q
     assert bcall(ptrs=P[:7] + [P[6]] + P[8:]) == fa.FA_ERR_ALIAS        # dk == dq
 
+    def tcall(ptrs=P, timeout_ns=0, D=64):
+        return fa.lib().fa_selftest_bwd_timeout(*ptrs, 1, 1, 128, 128, D, 0.125, 0, timeout_ns, 0)
+
+    assert tcall(timeout_ns=2_000_000_001) == fa.FA_ERR_BAD_SHAPE   # wait limit above 2 s
+    assert tcall(ptrs=[0] + P[1:]) == fa.FA_ERR_NULLPTR             # fa_bwd's checks apply
+    assert tcall(D=96) == fa.FA_ERR_UNSUPPORTED_D
+
 
 def test_fp8_argument_checks():
     def fcall(q=A, D=128, causal=0, Sq=128, Sk=128, scale=0.1, ds=(0.01, 0.01, 0.01), lse=A5,

@@ -148,6 +148,28 @@ def test_bwd_deterministic():
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
+def test_backward_kernels_give_up_cleanly():
+    """Both backward kernels' own give-up path: with every wait limited to 0 ns,
+    the first wait in progress when the global timer ticks gives up, raises its
+    CTA's abort flag and records FA_ERR_TIMEOUT; the other roles stop, copies and
+    MMAs in flight are waited for (bounded), TMEM is freed and the kernels
+    return.  The key and query sequences are long (8,192), so that a timer tick
+    falls inside some wait.  A normal backward after it must pass parity, so the
+    context is still usable."""
+    assert fa.fa_device_status() == fa.FA_OK
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 8192, 8192, 128, seed=41))
+    g = make_qkv(1, 2, 8192, 8192, 128, seed=42)[0].cuda()
+    o, lse = fa.fa_fwd(q, k, v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty_like(lse)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    assert fa.fa_selftest_bwd_timeout(q, k, v, o, lse, g, dq, dk, dv, delta, 128 ** -0.5, False, 0) == fa.FA_OK
+    assert fa.fa_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_device_status() == fa.FA_OK  # cleared by the read
+    _case(1, 2, 300, 300, 128, True, seed=43)
+
+
 def test_bwd_closed_form_sums_at_size():
     """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i (per head), up to bf16 rounding."""
     q, k, v = make_qkv(2, 4, 2048, 2048, 128, seed=8)
