@@ -15,7 +15,7 @@ import threading
 from . import build as _build
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_strerror", "fa_device_status",
-           "fa_selftest_bounded_wait", "fa_selftest_fwd_timeout", "fa_selftest_bwd_timeout", "fa_version", "FAError", "lib", "library_path",
+           "fa_selftest_bounded_wait", "fa_selftest_fwd_timeout", "fa_selftest_bwd_timeout", "fa_selftest_splitkv_timeout", "fa_version", "FAError", "lib", "library_path",
            "FA_OK", "FA_ERR_NULLPTR", "FA_ERR_BAD_SHAPE", "FA_ERR_UNSUPPORTED_D",
            "FA_ERR_UNSUPPORTED_CAUSAL", "FA_ERR_MISALIGNED", "FA_ERR_BAD_SCALE", "FA_ERR_CUDA",
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
@@ -64,6 +64,8 @@ _SIGNATURES = {
                                      _i, ctypes.c_ulonglong, _vp]),
     "fa_selftest_bwd_timeout": (_i, [_vp] * 10 + [_i, _i, _i, _i, _i, ctypes.c_float, _i, ctypes.c_ulonglong,
                                                   _vp]),
+    "fa_selftest_splitkv_timeout": (_i, [_vp] * 5 + [_i] * 5 + [ctypes.c_float, _i, _vp, ctypes.c_size_t,
+                                                               ctypes.c_ulonglong, _vp]),
     "fa_version": (_i, []),
 }
 
@@ -334,3 +336,17 @@ def fa_selftest_bwd_timeout(q, k, v, o, lse, dout, dq, dk, dv, delta, scale, cau
                                          lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                          dv.data_ptr(), delta.data_ptr(), B, H, Sq, Sk, D, float(scale),
                                          int(bool(causal)), int(timeout_ns), _stream_ptr(stream))
+
+
+def fa_selftest_splitkv_timeout(q, k, v, o, lse, workspace, scale, timeout_ns: int, num_splits: int = 0,
+                                stream=None) -> int:
+    """fa_fwd_splitkv with every on-chip wait of the partial kernel bounded by
+    `timeout_ns` (tests of the give-up path); returns the launch status.  All
+    arguments are contiguous CUDA tensors as for fa_fwd_splitkv; ``workspace`` is a
+    byte tensor of at least fa_fwd_splitkv_workspace_bytes."""
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    return lib().fa_selftest_splitkv_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                             lse.data_ptr(), B, H, Sq, Sk, D, float(scale), int(num_splits),
+                                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                             int(timeout_ns), _stream_ptr(stream))

@@ -294,9 +294,9 @@ extern "C" size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Sk, i
     return splitkv_bytes((long long)B * H, Sq, D, resolve_splits(B, H, Sk, num_splits));
 }
 
-extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                              int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
-                              size_t workspace_bytes, void *stream) {
+static int splitkv_checked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                           int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream, unsigned long long timeout_ns) {
     const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
     if (st != FA_OK) return st;
     if (Sq > fa::kSplitMaxSq || (long long)B * H > 65535 || num_splits > 256) return FA_ERR_BAD_SHAPE;
@@ -325,10 +325,26 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
     p.chunk = split_chunk(Sk, splits);
     p.splits = splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.timeout_ns = kWaitLimitNs;
+    p.timeout_ns = timeout_ns;
     const cudaError_t e = fa::launch_splitkv(D, tm_k, tm_v, p, (int)BH, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
+}
+
+extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                              int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return splitkv_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, num_splits, workspace, workspace_bytes, stream,
+                           kWaitLimitNs);
+}
+
+extern "C" int fa_selftest_splitkv_timeout(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                           int H, int Sq, int Sk, int D, float scale, int num_splits,
+                                           void *workspace, size_t workspace_bytes,
+                                           unsigned long long timeout_ns, void *stream) {
+    if (timeout_ns > kWaitLimitNs) return FA_ERR_BAD_SHAPE;
+    return splitkv_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, num_splits, workspace, workspace_bytes, stream,
+                           timeout_ns);
 }
 
 extern "C" int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,

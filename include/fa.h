@@ -285,6 +285,22 @@ int fa_selftest_bwd_timeout(const void *q, const void *k, const void *v, const v
                             int Sq, int Sk, int D, float scale, int causal, unsigned long long timeout_ns,
                             void *stream);
 
+/*
+ * fa_selftest_splitkv_timeout -- fa_fwd_splitkv with every on-chip wait of the
+ * partial kernel bounded by `timeout_ns` (0 .. 2e9) instead of 2 s.  With a
+ * limit shorter than a tile load the kernel gives up as the forward kernel
+ * does (abort flag, FA_ERR_TIMEOUT in the status word, copies in flight
+ * waited for, no trap); a CTA that gave up writes NaN as its partial
+ * log-sum-exp, so the merged O and LSE of its rows come out NaN instead of
+ * plausible stale values.  Arguments, checks and errors are fa_fwd_splitkv's,
+ * plus FA_ERR_BAD_SHAPE for timeout_ns above 2e9.  The surveyed pages have no
+ * counterpart: it exists so tests can show the decode kernels wind down
+ * cleanly and leave the context usable.
+ */
+int fa_selftest_splitkv_timeout(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                int H, int Sq, int Sk, int D, float scale, int num_splits, void *workspace,
+                                size_t workspace_bytes, unsigned long long timeout_ns, void *stream);
+
 /* fa_version -- library version, major*10000 + minor*100 + patch. */
 int fa_version(void);
 

@@ -177,6 +177,14 @@ def test_bwd_argument_checks():
     assert bcall(ptrs=P[:6] + [P[0] + 16] + P[7:]) == fa.FA_ERR_ALIAS   # dq over q
     assert bcall(ptrs=P[:7] + [P[6]] + P[8:]) == fa.FA_ERR_ALIAS        # dk == dq
 
+    def kcall(q=A, timeout_ns=0, ws=A2 + (1 << 24), wsb=1 << 20):
+        return fa.lib().fa_selftest_splitkv_timeout(q, A2, A3, A4, A5, 1, 1, 1, 128, 64, 0.125, 0, ws, wsb,
+                                                    timeout_ns, 0)
+
+    assert kcall(timeout_ns=2_000_000_001) == fa.FA_ERR_BAD_SHAPE   # wait limit above 2 s
+    assert kcall(q=0) == fa.FA_ERR_NULLPTR                            # fa_fwd_splitkv's checks apply
+    assert kcall(ws=0) == fa.FA_ERR_WORKSPACE
+
     def tcall(ptrs=P, timeout_ns=0, D=64):
         return fa.lib().fa_selftest_bwd_timeout(*ptrs, 1, 1, 128, 128, D, 0.125, 0, timeout_ns, 0)
 

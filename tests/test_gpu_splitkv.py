@@ -74,3 +74,32 @@ def test_splitkv_rejects_short_workspace_on_device():
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd_splitkv(q, k, v, workspace=ws)
     assert e.value.status == fa.FA_ERR_WORKSPACE
+
+
+def test_splitkv_kernel_gives_up_cleanly():
+    """The decode kernels' give-up path: with every wait of the partial kernel
+    limited to 0 ns (four splits of 16,384 keys, so that a timer tick falls
+    inside some wait), FA_ERR_TIMEOUT is recorded, and every output row is
+    either exactly what a normal call gives (all of its splits finished) or NaN
+    (a split gave up and marked its partial invalid) -- never a blend of stale
+    workspace bytes.  A normal call after it must pass parity."""
+    q, k, v = make_qkv(2, 4, 1, 65536, 128, seed=51)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = fa.fa_fwd_splitkv(qd, kd, vd, num_splits=4)
+    need = fa.fa_fwd_splitkv_workspace_bytes(2, 4, 1, 65536, 128, 4)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    o, lse = torch.empty_like(o_ref), torch.empty_like(lse_ref)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    assert fa.fa_selftest_splitkv_timeout(qd, kd, vd, o, lse, ws, 128 ** -0.5, 0, num_splits=4) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_device_status() == fa.FA_OK  # cleared by the read
+    nan_rows = torch.isnan(lse)
+    assert nan_rows.any()
+    assert torch.equal(lse[~nan_rows], lse_ref[~nan_rows])
+    assert torch.equal(o[~nan_rows], o_ref[~nan_rows])
+    assert torch.isnan(o[nan_rows].float()).all()
+    qs, ks, vs = make_qkv(1, 2, 3, 3000, 128, seed=52)
+    og, lg = run_gpu(qs, ks, vs, 128 ** -0.5, False, splits=0)
+    compare(og, lg, *oracle.attn_fwd(*(bf16_bits(t) for t in (qs, ks, vs)), 128 ** -0.5, False), "after timeout")
