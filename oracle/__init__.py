@@ -176,6 +176,59 @@ def attn_fwd_tiled(q, k, v, scale: float, causal: bool = False, window=(-1, -1),
     return o, lse
 
 
+def attn_fwd_blockmask(q, k, v, scale: float, block_mask, window=(-1, -1), block=(128, 128)):
+    """Attention over the keys that a block mask keeps, in fp64 (numpy).
+
+    "FlashAttention-2 -- L3 Cross-Paper Synthesis", section 5 item 4: the causal
+    block skip generalises to sliding windows and dilated patterns, one
+    sparse-block-skip mechanism.  The pages define no pattern beyond the window,
+    so the mechanism is taken as given by the caller: ``block_mask[h, a, c]``
+    nonzero keeps key block ``c`` (keys ``c*bn .. c*bn+bn-1``) for query block
+    ``a`` (rows ``a*bm .. a*bm+bm-1``) of head ``h``.  Key ``j`` is allowed for
+    query ``i`` iff ``j < Sk``, the window keeps it (``i-wl <= j <= i+wr``, a
+    negative bound unbounded; causal is ``(-1, 0)``) and its block is kept.
+
+    ``q, k, v``: ``[B,H,S,D]`` float64, or uint16 bf16 bit patterns (widened
+    exactly).  ``block_mask``: ``[Hm, ceil(Sq/bm), ceil(Sk/bn)]`` with ``Hm``
+    1 (one pattern for every head) or ``B*H`` (head ``b*H+h``).
+
+    The definition written out: S = scale Q K^T, S = -inf where not allowed,
+    P = softmax over the row, O = P V, LSE = ln sum exp S.  A row with no
+    allowed key gets O = 0 and LSE = -inf (a reading: with every key masked the
+    row takes no value from V, and its log-sum-exp is that of an empty sum).
+    Returns (O float64 [B,H,Sq,D], LSE float64 [B,H,Sq]).
+    """
+    q, k, v, B, H, Sq, Sk, D = _prep(q, k, v)
+    if q.dtype == np.uint16:
+        q, k, v = (bf16_bits_to_f64(x) for x in (q, k, v))
+    bm, bn = int(block[0]), int(block[1])
+    mask = np.asarray(block_mask)
+    n_qb, n_kb = -(-Sq // bm), -(-Sk // bn)
+    if mask.ndim != 3 or mask.shape[1:] != (n_qb, n_kb) or mask.shape[0] not in (1, B * H):
+        raise ValueError(f"block_mask must be [1 or B*H, {n_qb}, {n_kb}], got {mask.shape}")
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    band = np.ones((Sq, Sk), bool)
+    if window[0] >= 0:
+        band &= j >= i - window[0]
+    if window[1] >= 0:
+        band &= j <= i + window[1]
+    o = np.zeros((B, H, Sq, D), np.float64)
+    lse = np.full((B, H, Sq), -np.inf)
+    for bh in range(B * H):
+        b, h = divmod(bh, H)
+        kept = mask[0 if mask.shape[0] == 1 else bh] != 0
+        allowed = band & kept[np.arange(Sq) // bm][:, np.arange(Sk) // bn]
+        s = np.where(allowed, float(scale) * (q[b, h] @ k[b, h].T), -np.inf)
+        m = s.max(axis=1)
+        live = m > -np.inf
+        p = np.exp(s[live] - m[live, None])
+        l = p.sum(axis=1)
+        o[b, h, live] = (p @ v[b, h]) / l[:, None]
+        lse[b, h, live] = m[live] + np.log(l)
+    return o, lse
+
+
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact widening of uint16 bf16 bit patterns to float64 (for tests)."""
     u32 = np.asarray(bits, np.uint16).astype(np.uint32) << 16
