@@ -21,7 +21,8 @@ __all__ = ["fa_fwd", "fa_fwd_raw", "fa_fwd_window", "fa_fwd_window_raw", "fa_str
            "FA_ERR_TIMEOUT", "FA_ERR_ALIAS", "FA_ERR_BAD_WINDOW", "FA_ERR_WORKSPACE",
            "fa_fwd_splitkv", "fa_fwd_splitkv_raw", "fa_fwd_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "FA_ERR_SCRATCH_LIMIT",
-           "fa_bwd", "fa_bwd_raw", "fa_fwd_fp8", "fa_fwd_fp8_raw"]
+           "fa_bwd", "fa_bwd_raw", "fa_fwd_fp8", "fa_fwd_fp8_raw",
+           "fa_fwd_blockmask", "fa_fwd_blockmask_raw", "FA_ERR_BAD_MASK", "FA_BLOCK_M", "FA_BLOCK_N"]
 
 FA_OK = 0
 FA_ERR_NULLPTR = -1
@@ -36,6 +37,9 @@ FA_ERR_ALIAS = -9
 FA_ERR_BAD_WINDOW = -10
 FA_ERR_WORKSPACE = -11
 FA_ERR_SCRATCH_LIMIT = -12
+FA_ERR_BAD_MASK = -13
+FA_BLOCK_M = 128  # query rows per block-mask row
+FA_BLOCK_N = 128  # keys per block-mask column
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +52,8 @@ _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]),
     "fa_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
                            _vp]),
+    "fa_fwd_blockmask": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
+                              _vp, _i, _vp]),
     "fa_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp,
                             ctypes.c_size_t, _vp]),
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
@@ -129,6 +135,15 @@ def fa_fwd_window_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: i
                                int(window_left), int(window_right), stream_ptr)
 
 
+def fa_fwd_blockmask_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                         H: int, Sq: int, Sk: int, D: int, scale: float, window_left: int,
+                         window_right: int, mask_ptr: int, mask_heads: int, stream_ptr: int) -> int:
+    """The block-mask C call with raw device pointers; returns the status code."""
+    return lib().fa_fwd_blockmask(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
+                                  int(window_left), int(window_right), mask_ptr, int(mask_heads),
+                                  stream_ptr)
+
+
 def _prepare(q, k, v, o, lse):
     import torch
 
@@ -181,6 +196,30 @@ def fa_fwd_window(q, k, v, window_left: int, window_right: int, o=None, lse=None
                            _stream_ptr(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_window")
+    return o, lse
+
+
+def fa_fwd_blockmask(q, k, v, block_mask, window_left: int = -1, window_right: int = -1, o=None,
+                     lse=None, scale: float | None = None, stream=None):
+    """Attention over the key blocks ``block_mask`` keeps (uint8 or bool CUDA tensor
+    ``[mask_heads, ceil(Sq/128), ceil(Sk/128)]``, ``mask_heads`` 1 or B*H; nonzero
+    keeps a 128-row x 128-key block), within the band of fa_fwd_window.  Rows with
+    no allowed key get O = 0, LSE = -inf.  Same tensors and return value as fa_fwd."""
+    import torch
+
+    o, lse, B, H, Sq, Sk, D = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = D ** -0.5
+    n_qb, n_kb = -(-Sq // FA_BLOCK_M), -(-Sk // FA_BLOCK_N)
+    if (block_mask.dtype not in (torch.uint8, torch.bool) or not block_mask.is_cuda
+            or not block_mask.is_contiguous() or block_mask.dim() != 3
+            or tuple(block_mask.shape[1:]) != (n_qb, n_kb)):
+        raise ValueError(f"block_mask must be a contiguous CUDA uint8/bool tensor [mask_heads, {n_qb}, {n_kb}]")
+    st = fa_fwd_blockmask_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, Sq, Sk, D, scale, window_left, window_right,
+                              block_mask.data_ptr(), block_mask.shape[0], _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_blockmask")
     return o, lse
 
 

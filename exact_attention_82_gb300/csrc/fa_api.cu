@@ -89,6 +89,7 @@ extern "C" const char *fa_strerror(int status) {
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
         case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1, and a bounded window needs Sq == Sk"; break;
         case FA_ERR_WORKSPACE: s = "workspace missing, not 16-byte aligned, or smaller than required"; break;
+        case FA_ERR_BAD_MASK: s = "mask_heads must be 1 or B * H"; break;
         case FA_ERR_SCRATCH_LIMIT:
             s = "needs more scratch than the built-in 16 MiB buffer of fa_fwd_splitkv_noalloc holds; "
                 "pass a workspace to fa_fwd_splitkv instead";
@@ -142,7 +143,8 @@ static int check_fwd(const void *q, const void *k, const void *v, const void *o,
 // for query i iff i - wl <= j <= i + wr (a negative bound: unbounded).
 static int launch_checked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
                           int Sk, int D, float scale, int wl, int wr, void *stream,
-                          unsigned long long timeout_ns = kWaitLimitNs) {
+                          unsigned long long timeout_ns = kWaitLimitNs, const unsigned char *bmask = nullptr,
+                          long long bmask_hstride = 0) {
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
     const long long BH = (long long)B * H;
     const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
@@ -165,6 +167,8 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.o_scale = 1.f;
     p.timeout_ns = timeout_ns;
+    p.bmask = bmask;
+    p.bmask_hstride = bmask_hstride;
     const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
@@ -187,6 +191,25 @@ extern "C" int fa_fwd_window(const void *q, const void *k, const void *v, void *
     if (window_left < -1 || window_right < -1) return FA_ERR_BAD_WINDOW;
     if ((window_left >= 0 || window_right >= 0) && Sq != Sk) return FA_ERR_BAD_WINDOW;
     return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream);
+}
+
+extern "C" int fa_fwd_blockmask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                int Sq, int Sk, int D, float scale, int window_left, int window_right,
+                                const unsigned char *block_mask, int mask_heads, void *stream) {
+    const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
+    if (st != FA_OK) return st;
+    if (!block_mask) return FA_ERR_NULLPTR;
+    if (window_left < -1 || window_right < -1) return FA_ERR_BAD_WINDOW;
+    if ((window_left >= 0 || window_right >= 0) && Sq != Sk) return FA_ERR_BAD_WINDOW;
+    const long long BH = (long long)B * H;
+    if (mask_heads != 1 && (long long)mask_heads != BH) return FA_ERR_BAD_MASK;
+    const long long n_qb = (Sq + fa::kBlockM - 1) / fa::kBlockM, n_kb = (Sk + fa::kBlockN - 1) / fa::kBlockN;
+    const size_t mask_bytes = (size_t)mask_heads * (size_t)(n_qb * n_kb);
+    const size_t o_bytes = (size_t)BH * Sq * D * 2, lse_bytes = (size_t)BH * Sq * 4;
+    if (overlaps(block_mask, mask_bytes, o, o_bytes) || overlaps(block_mask, mask_bytes, lse, lse_bytes))
+        return FA_ERR_ALIAS;
+    return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream, kWaitLimitNs,
+                          block_mask, mask_heads == 1 ? 0 : n_qb * n_kb);
 }
 
 extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
@@ -233,6 +256,8 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
     p.scale_log2 = scale_log2;
     p.o_scale = descale_v;
     p.timeout_ns = kWaitLimitNs;
+    p.bmask = nullptr;
+    p.bmask_hstride = 0;
     const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;

@@ -180,6 +180,12 @@ struct Item {
     int jhi[2], jlo[2];
     int J, N;
     int first[2], last[2];
+    // Block mask (banded kernel): mrow[t] is sub-tile t's row of the mask (null:
+    // no mask, every tile of its range taken).  A sub-tile whose row keeps no
+    // tile of its range takes part in one tile with every key masked ("none"),
+    // so that its rows come out as O = 0, LSE = -inf through the usual path.
+    const unsigned char *mrow[2];
+    bool none[2];
 };
 
 // The r-th item of this CTA: items are dealt out in rounds of gridDim.x in
@@ -191,7 +197,7 @@ __device__ __forceinline__ int item_index(int r) {
     return r * G + ((r & 1) ? G - 1 - b : b);
 }
 
-template <bool WIN>
+template <bool WIN, bool MASK>
 __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
     Item g;
     int mi;
@@ -212,8 +218,39 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
         g.jlo[t] = (WIN && p.wl >= 0) ? max(0, (r_first - p.wl) / kBlockN) : 0;
     }
     g.act1 = g.row0 + kBlockM < p.Sq;
+    g.mrow[0] = g.mrow[1] = nullptr;
+    g.none[0] = g.none[1] = false;
+    if constexpr (MASK) {
+        {
+            // each sub-tile's range shrinks to the tiles its mask row keeps
+            const unsigned char *mh = p.bmask + (size_t)g.bh * (size_t)p.bmask_hstride;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (t == 1 && !g.act1) break;
+                const unsigned char *mr = mh + (size_t)(2 * mblk + t) * (size_t)p.n_kv;
+                int hi = -1, lo = -1;
+                for (int j = g.jhi[t]; j >= g.jlo[t]; --j)
+                    if (mr[j]) {
+                        if (hi < 0) hi = j;
+                        lo = j;
+                    }
+                g.mrow[t] = mr;
+                g.none[t] = hi < 0;
+                g.jhi[t] = hi;
+                g.jlo[t] = lo;
+            }
+            // a sub-tile that keeps nothing rides along on the other's first tile
+            // (tile 0 when neither keeps anything)
+            const bool live1 = g.act1 && !g.none[1];
+            if (g.none[0]) g.jhi[0] = g.jlo[0] = live1 ? g.jhi[1] : 0;
+            if (g.act1 && g.none[1]) g.jhi[1] = g.jlo[1] = g.jhi[0];
+        }
+    }
     g.J = g.act1 ? max(g.jhi[0], g.jhi[1]) : g.jhi[0];
-    g.N = g.J - g.jlo[0] + 1;  // sub-tile 0 reaches lowest
+    if constexpr (MASK)
+        g.N = g.J - (g.act1 ? min(g.jlo[0], g.jlo[1]) : g.jlo[0]) + 1;
+    else
+        g.N = g.J - g.jlo[0] + 1;  // sub-tile 0 reaches lowest
     g.first[0] = g.J - g.jhi[0];
     g.last[0] = g.J - g.jlo[0];
     g.first[1] = g.act1 ? g.J - g.jhi[1] : g.N;
@@ -221,11 +258,49 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
     return g;
 }
 
+// Does sub-tile t of item g take part in load-order tile `it`?  Without a block
+// mask: every tile of its range; with one: the tiles its mask row keeps.
+template <bool MASK>
+__device__ __forceinline__ bool takes_part(const Item &g, int t, int it) {
+    if (it < g.first[t] || it > g.last[t]) return false;
+    if constexpr (MASK) {
+        if (!g.none[t]) return g.mrow[t][g.J - it] != 0;
+    }
+    return true;
+}
+// Is load-order tile `it` loaded at all (some sub-tile takes part)?
+template <bool MASK>
+__device__ __forceinline__ bool tile_live(const Item &g, int it) {
+    return takes_part<MASK>(g, 0, it) || takes_part<MASK>(g, 1, it);
+}
+// The next load-order tile after `it` that is loaded (g.N if none).
+template <bool MASK>
+__device__ __forceinline__ int next_live(const Item &g, int it) {
+    if constexpr (MASK) {
+        do {
+            ++it;
+        } while (it < g.N && !tile_live<MASK>(g, it));
+        return it;
+    } else {
+        return it + 1;
+    }
+}
+
 // WIN: a bounded key band (window_left >= 0 or window_right > 0).  Without it
 // (full or causal attention) only a sub-tile's first key tile can need a mask
 // and every row has an allowed key in it, which the code below exploits.
 // F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
-template <int D, bool WIN, bool F8>
+// MASK (with WIN): a block mask keeps, per 128-row query block, a set of 128-key
+// tiles ("FlashAttention-2 — L3 Cross-Paper Synthesis", §5 item 4: causal block
+// skipping generalised into one sparse-block-skip mechanism).  An item's two
+// sub-tiles still share one K/V stream -- the tiles either of them keeps, in the
+// same descending order; tiles neither keeps are never loaded -- and each
+// sub-tile takes part only in its own tiles, so its S, P and P V run on those
+// alone.  A sub-tile that keeps nothing rides along on one loaded tile with
+// every key masked, which gives its rows O = 0 and LSE = -inf through the
+// banded path's handling of rows without a key.  (A separate instantiation: the
+// scan of the mask, even untaken, slowed the plain banded kernel by 11%.)
+template <int D, bool WIN, bool F8, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -341,16 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
-                const Item g = item_at<WIN>(p, k);
+                const Item g = item_at<WIN, MASK>(p, k);
                 if constexpr (QB == 3) {
                     // this item's Q_0 was loaded one item ahead (below), except the first
                     if (r == 0) ok = load_q_ring(g, 0);
                     if (ok && g.act1) ok = load_q_ring(g, 1);
                     if (ok) ok = load_k(g, 0);
                     const int kn = item_index(r + 1);
-                    if (ok && kn < p.n_items) ok = load_q_ring(item_at<WIN>(p, kn), 0);
-                    for (int it = 0; ok && it < g.N; ++it) {
-                        if (it + 1 < g.N) ok = load_k(g, it + 1);
+                    if (ok && kn < p.n_items) ok = load_q_ring(item_at<WIN, MASK>(p, kn), 0);
+                    for (int it = 0, nx; ok && it < g.N; it = nx) {  // tiles no sub-tile takes are skipped
+                        nx = next_live<MASK>(g, it);
+                        if (nx < g.N) ok = load_k(g, nx);
                         if (ok) ok = load_v(g, it);
                     }
                     continue;
@@ -370,8 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 ok = load_q(0, qn0) && (!g.act1 || load_q(1, qn1));
                 if (ok) ok = load_k(g, 0);
-                for (int it = 0; ok && it < g.N; ++it) {
-                    if (it + 1 < g.N) ok = load_k(g, it + 1);
+                for (int it = 0, nx; ok && it < g.N; it = nx) {
+                    nx = next_live<MASK>(g, it);
+                    if (nx < g.N) ok = load_k(g, nx);
                     if (ok) ok = load_v(g, it);
                 }
             }
@@ -497,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return pv_sepp(t, pd.first, pd.stage, pd.phase);
                 };
                 for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
-                    const Item g = item_at<WIN>(p, k);
+                    const Item g = item_at<WIN, MASK>(p, k);
                     const int qb0 = 2 * (qn0 % QB), qb1 = 2 * (qn1 % QB) + 1;
                     qfb0 = B_Q_FULL + qb0;
                     qfb1 = B_Q_FULL + qb1;
@@ -505,10 +582,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qfp1 = (uint32_t)(qn1 / QB) & 1u;
                     const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
                     for (int it = 0; ok && it < g.N; ++it) {
+                        if constexpr (MASK) {
+                            if (!tile_live<MASK>(g, it)) continue;  // not loaded: no sub-tile keeps it
+                        }
                         ok = wait(B_K_FULL + sk, kph);
                         if (!ok) break;
-                        const bool p0 = it >= g.first[0] && it <= g.last[0];
-                        const bool p1 = it >= g.first[1] && it <= g.last[1];
+                        const bool p0 = takes_part<MASK>(g, 0, it);
+                        const bool p1 = takes_part<MASK>(g, 1, it);
                         if (p0) {
                             if (it == g.first[0]) ok = q_ready(0);
                             if (ok && ns0 > 0) ok = wait(B_S_FREE + 0, (uint32_t)(ns0 - 1) & 1u);
@@ -547,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && vpend) tc_commit(bar(B_V_EMPTY + svp));
             } else {
                 for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
-                    const Item g = item_at<WIN>(p, k);
+                    const Item g = item_at<WIN, MASK>(p, k);
                     const int first0 = g.first[0], last0 = g.last[0], first1 = g.first[1], last1 = g.last[1];
                     const int N = g.N;
                     // this item's query buffers (slots), their descriptors and barriers:
@@ -591,13 +671,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                             return true;
                         };
                         bool kready = false;  // K_FULL of key tile `it` already waited for
+                        bool prev1 = false;   // (block mask) sub-tile 1 took part in the previous loaded tile
+                        int prev_it = -1;     // (block mask) that tile
                         for (int it = 0; ok && it < N; ++it) {
+                            if constexpr (MASK) {
+                                if (!tile_live<MASK>(g, it)) continue;  // not loaded: no sub-tile keeps it
+                            }
                             if (!kready) ok = wait(B_K_FULL + sk, kph);
                             kready = false;
                             if (!ok) break;
                             tc_fence_after();
-                            const bool p0 = it >= first0 && it <= last0;
-                            const bool p1 = it >= first1 && it <= last1;
+                            const bool p0 = takes_part<MASK>(g, 0, it);
+                            const bool p1 = takes_part<MASK>(g, 1, it);
+                            // sub-tile 1 took part in the previous tile, and whether that was its last
+                            const bool pv1 = MASK ? prev1 : (it > first1 && it - 1 <= last1);
+                            const bool pv1_last = MASK ? prev_it == last1 : it - 1 == last1;
                             if (p0) {
                                 if (it == first0) {
                                     ok = q_ready(0);
@@ -608,10 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_commit(bar(B_S_FULL + 0));
                                 if (it == last0) tc_commit(bar(qf0));
                             }
-                            if (it > first1 && it - 1 <= last1) {  // sub-tile 1 took part in the previous tile
+                            if (pv1) {
                                 ok = issue_pv(1, ipv1++, svp, vpph);
                                 if (!ok) break;
-                                if (it - 1 == last1) tc_commit(bar(B_O_DONE + 1));
+                                if (pv1_last) tc_commit(bar(B_O_DONE + 1));
                                 tc_commit(bar(B_V_EMPTY + svp));
                             }
                             if (p1) {
@@ -627,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_commit(bar(B_K_EMPTY + sk));
                             // the next key tile's K is waited for here, so that P0 V and
                             // the next S0 issue back to back (S0 then waits on nothing)
-                            if (it + 1 < N) {
+                            if (next_live<MASK>(g, it) < N) {
                                 ok = wait(B_K_FULL + (sk + 1 == C::KST ? 0 : sk + 1), sk + 1 == C::KST ? kph ^ 1u : kph);
                                 if (!ok) break;
                                 kready = true;
@@ -642,8 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             svp = sv;
                             vpph = vph;
                             if (++sv == C::VST) { sv = 0; vph ^= 1u; }
+                            prev1 = p1;
+                            prev_it = it;
                         }
-                        if (ok && last1 == N - 1) {
+                        if (ok && (MASK ? prev1 : last1 == N - 1)) {
                             ok = issue_pv(1, ipv1, svp, vpph);
                             if (ok) {
                                 tc_commit(bar(B_O_DONE + 1));
@@ -685,8 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stores), and LSE; rows >= Sq are not written
         auto store_row = [&](const uint32_t (&o)[D / 32][32], float m, float l, int rg, int bh) {
             if (rg >= p.Sq) return;
-            // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels)
-            const float inv_l = (F8 ? p.o_scale : 1.f) / l;
+            // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels).
+            // A banded row with no allowed key (l = 0, O = 0): O = 0, LSE = -inf.
+            const float inv_l = (MASK && !(l > 0.f)) ? 0.f : (F8 ? p.o_scale : 1.f) / l;
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + ((size_t)bh * p.Sq + rg) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c)
@@ -699,7 +790,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
                     dst[c * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            p.lse[(size_t)bh * p.Sq + rg] = (m - (F8 ? kF8PShift : 0.f) + lg2_approx(l)) * 0.69314718055994531f;
+            p.lse[(size_t)bh * p.Sq + rg] = (MASK && !(l > 0.f))
+                                                ? -INFINITY
+                                                : (m - (F8 ? kF8PShift : 0.f) + lg2_approx(l)) * 0.69314718055994531f;
         };
         // Each thread stores its own O row straight from registers, so a sub-tile's
         // Q buffer can take the next item's Q as early as possible.
@@ -708,12 +801,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY;  // max in exp2 units (raw score * scale*log2e) used for P
         float l_run = 0.f;         // sum of P over the keys seen, relative to m_used
         for (int r = 0, k = item_index(0); ok && k < p.n_items; k = item_index(++r)) {
-            g = item_at<WIN>(p, k);
+            g = item_at<WIN, MASK>(p, k);
             if (t == 1 && !g.act1) continue;
             const int my_jhi = t ? g.jhi[1] : g.jhi[0], my_jlo = t ? g.jlo[1] : g.jlo[0];
             const int r_first = g.row0 + t * C::BM, r_last = r_first + C::BM - 1;
             const int row_g = r_first + row;
-            const int n_t = my_jhi - my_jlo + 1;
+            int n_t = my_jhi - my_jlo + 1;
+            // block mask: the tiles of [my_jlo, my_jhi] this sub-tile's row keeps,
+            // visited from the highest (jt steps down to each in turn)
+            const bool none = MASK && (t ? g.none[1] : g.none[0]);
+            const unsigned char *mrow = (MASK && !none) ? (t ? g.mrow[1] : g.mrow[0]) : nullptr;
+            if constexpr (MASK) {
+                if (mrow) {
+                    n_t = 0;
+                    for (int j = my_jlo; j <= my_jhi; ++j) n_t += mrow[j] != 0;
+                }
+            }
+            int jt = my_jhi + 1;
             // allowed keys of this row: [k_lo, k_hi)
             const int k_lo = (p.wl >= 0) ? row_g - p.wl : 0;
             const int k_hi = (p.wr >= 0) ? min(p.Sk, row_g + p.wr + 1) : p.Sk;
@@ -736,11 +840,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(s_tm + 96, s[3]);
                 // A tile needs the mask unless every row of the sub-tile may see all
                 // of its keys (causal: only the diagonal tile; ragged: the last).
-                const int col0 = (my_jhi - i) * C::BN;
-                const bool masked = WIN ? (col0 + C::BN > p.Sk || (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
+                // A sub-tile whose block-mask row keeps nothing masks every key.
+                if constexpr (MASK) {
+                    do {
+                        --jt;
+                    } while (mrow && !mrow[jt]);
+                }
+                const int col0 = (MASK ? jt : my_jhi - i) * C::BN;
+                const bool masked = WIN ? ((MASK && none) || col0 + C::BN > p.Sk ||
+                                           (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
                                            (p.wl >= 0 && col0 < r_last - p.wl))
                                         : (i == 0 && (p.wr >= 0 || (p.Sk % C::BN) != 0));
-                const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
+                const int lim_lo = (MASK && none) ? 0 : k_lo - col0, lim_hi = (MASK && none) ? 0 : k_hi - col0;
                 if (F8 || masked || (WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : i == 0))
                     tmem_ld_wait2(s[2], s[3]);
                 if constexpr (C::P_SMEM) {
@@ -1108,24 +1219,27 @@ __global__ void fa_wait_selftest(unsigned long long limit_ns) {
     __syncthreads();
 }
 
-template <int D, bool WIN, bool F8>
+template <int D, bool WIN, bool F8, bool MASK = false>
 static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const FwdParams &p, int num_sms, cudaStream_t stream) {
     constexpr uint32_t smem = FwdCfg<D, F8, query_buffers(D, F8)>::SMEM;
     cudaError_t e =
-        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fa_fwd_sm103a<D, WIN, F8, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // Persistent CTAs (at most one per SM, each walking many items) take the
     // fixed cost of a CTA off every item but the first and even out items of
     // different length (causal: longest first, dealt out in snake order).
     const int n_ctas = p.n_items > num_sms ? num_sms : p.n_items;
-    fa_fwd_sm103a<D, WIN, F8><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, p);
+    fa_fwd_sm103a<D, WIN, F8, MASK><<<dim3((unsigned)n_ctas), dim3(kThreads), smem, stream>>>(tm_q, tm_k, tm_v, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const FwdParams &p, int num_sms, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
+    if (p.bmask)  // a block mask runs on the banded kernel's masking and empty-row handling
+        return D == 64 ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream)
+                       : launch_fwd_d<128, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream);
     if (D == 64)
         return win ? launch_fwd_d<64, true, false>(tm_q, tm_k, tm_v, p, num_sms, stream)
                    : launch_fwd_d<64, false, false>(tm_q, tm_k, tm_v, p, num_sms, stream);

@@ -25,6 +25,11 @@ struct FwdParams {
     float scale_log2;  // scale * log2(e)  (8-bit path: times descale_q * descale_k)
     float o_scale;     // 8-bit path: descale_v (unused by the bf16 path)
     unsigned long long timeout_ns;  // bound of every on-chip wait
+    // Block mask (banded kernel only; null: every block kept): bmask[h][a][c]
+    // nonzero keeps key tile c for 128-row query block a of head h, where h is
+    // the head for bmask_hstride = n_qb * n_kv and 0 for bmask_hstride = 0.
+    const unsigned char *bmask;
+    long long bmask_hstride;
 };
 
 // Split-KV (decode) launch: partials per (head, split), then a merge.

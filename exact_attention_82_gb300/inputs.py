@@ -162,3 +162,25 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bit patterns (uint16 numpy) of a bf16 CPU tensor, for the oracle."""
     assert t.dtype == torch.bfloat16
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def random_block_mask(heads: int, n_qb: int, n_kb: int, keep: float, seed: int) -> torch.Tensor:
+    """uint8 CPU block mask [heads, n_qb, n_kb]: each block kept with probability
+    ``keep``, drawn from one seeded generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return (torch.rand((heads, n_qb, n_kb), generator=g) < keep).to(torch.uint8)
+
+
+def dilated_block_mask(n_qb: int, n_kb: int, stride: int, causal: bool = False) -> torch.Tensor:
+    """uint8 CPU block mask [1, n_qb, n_kb] of a dilated block pattern: query block a
+    keeps key block c iff (a - c) is a multiple of ``stride`` (and c <= a when
+    ``causal``).  The pages name dilated patterns beside sliding windows without
+    defining one; this is the plainest block-level reading (every stride-th block
+    counted from the diagonal), not a pattern the pages fix."""
+    a = torch.arange(n_qb).view(-1, 1)
+    c = torch.arange(n_kb).view(1, -1)
+    keep = (a - c) % stride == 0
+    if causal:
+        keep &= c <= a
+    return keep.to(torch.uint8).unsqueeze(0).contiguous()

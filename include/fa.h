@@ -53,7 +53,8 @@ typedef enum {
     FA_ERR_ALIAS = -9,              /* an output overlaps an input or the other one */
     FA_ERR_BAD_WINDOW = -10,        /* window bound below -1, or band with Sq != Sk  */
     FA_ERR_WORKSPACE = -11,         /* workspace missing, misaligned or too small    */
-    FA_ERR_SCRATCH_LIMIT = -12      /* more scratch than the built-in buffer holds   */
+    FA_ERR_SCRATCH_LIMIT = -12,     /* more scratch than the built-in buffer holds   */
+    FA_ERR_BAD_MASK = -13           /* block mask heads other than 1 or B * H        */
 } fa_status;
 
 /*
@@ -101,6 +102,35 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                   int Sq, int Sk, int D, float scale, int window_left, int window_right,
                   void *stream);
+
+/*
+ * fa_fwd_blockmask -- attention forward over the key blocks a block mask keeps:
+ * the "unified sparse-block-skip mechanism" into which "FlashAttention-2 — L3
+ * Cross-Paper Synthesis", §5 item 4, generalises causal block skipping (the
+ * sliding window and dilated patterns being instances).  Key j is allowed for
+ * query i iff j < Sk, the band keeps it (i - window_left <= j <= i +
+ * window_right, as in fa_fwd_window: -1 unbounded, (-1, 0) causal) and
+ *     block_mask[m][i / FA_BLOCK_M][j / FA_BLOCK_N] != 0,
+ * where m = 0 when mask_heads = 1 (one pattern for every head) and m = b*H + h
+ * when mask_heads = B * H.  Key blocks a query block does not keep are never
+ * loaded or multiplied.
+ *
+ *   block_mask  uint8 [mask_heads, ceil(Sq / FA_BLOCK_M), ceil(Sk / FA_BLOCK_N)]
+ *               DEVICE pointer, read by the kernel (must stay valid until the
+ *               stream passes it), any alignment, must not overlap O or LSE
+ *   mask_heads  1 or B * H
+ * Other arguments, layout, ownership and outputs are those of fa_fwd_window.
+ * A query row with no allowed key (its block row keeps nothing, or the band
+ * leaves nothing of what it keeps) gets O = 0 and LSE = -inf.
+ * Errors: those of fa_fwd_window, plus FA_ERR_NULLPTR for a null mask,
+ * FA_ERR_BAD_MASK for mask_heads other than 1 or B * H, and FA_ERR_ALIAS when
+ * the mask overlaps O or LSE.  With every block kept it equals fa_fwd_window.
+ */
+#define FA_BLOCK_M 128
+#define FA_BLOCK_N 128
+int fa_fwd_blockmask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                     int Sq, int Sk, int D, float scale, int window_left, int window_right,
+                     const unsigned char *block_mask, int mask_heads, void *stream);
 
 /*
  * fa_fwd_fp8 -- attention forward with 8-bit (e4m3) Q, K, V and per-tensor

@@ -49,7 +49,7 @@ def test_library_is_in_tree():
 
 def test_version_and_strerror():
     assert fa.fa_version() >= 100
-    for code in range(0, -13, -1):
+    for code in range(0, -14, -1):
         s = fa.fa_strerror(code)
         assert s and s != "unknown status", code
     assert fa.fa_strerror(12345) == "unknown status"
@@ -129,6 +129,31 @@ def test_window_argument_checks():
         fa.FA_ERR_NULLPTR
     assert fa.fa_fwd_window_raw(A, A2, A3, A4, A5, 1, 1, 128, 128, 96, 0.125, 4, 0, 0) == \
         fa.FA_ERR_UNSUPPORTED_D
+
+
+def mcall(mask=1 << 42, heads=1, B=1, H=1, Sq=300, Sk=300, wl=-1, wr=-1, o=A4, lse=A5, D=64):
+    return fa.fa_fwd_blockmask_raw(A, A2, A3, o, lse, B, H, Sq, Sk, D, 0.125, wl, wr, mask, heads, 0)
+
+
+def test_blockmask_argument_checks():
+    assert mcall(mask=0) == fa.FA_ERR_NULLPTR
+    assert mcall(heads=2, B=1, H=3) == fa.FA_ERR_BAD_MASK
+    assert mcall(heads=0) == fa.FA_ERR_BAD_MASK
+    assert mcall(wl=-2) == fa.FA_ERR_BAD_WINDOW
+    assert mcall(wl=16, wr=0, Sq=128, Sk=256) == fa.FA_ERR_BAD_WINDOW
+    assert mcall(D=96) == fa.FA_ERR_UNSUPPORTED_D
+    # the mask may not overlap O (bytes [A4, A4 + 300*64*2)) or LSE
+    assert mcall(mask=A4 + 100) == fa.FA_ERR_ALIAS
+    assert mcall(mask=A5 + 4) == fa.FA_ERR_ALIAS
+    # one byte before O with a mask of 3 x 3 blocks overlaps it
+    assert mcall(mask=A4 - 1) == fa.FA_ERR_ALIAS
+    assert "mask" in fa.fa_strerror(fa.FA_ERR_BAD_MASK)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path only")
+def test_blockmask_valid_call_without_gpu_reports_cuda_error():
+    assert mcall(heads=3, B=1, H=3) == fa.FA_ERR_CUDA
+    assert mcall(mask=A4 - 9) == fa.FA_ERR_CUDA  # 9 bytes of mask end right before O
 
 
 def test_splitkv_sizes_and_checks():
