@@ -186,7 +186,28 @@ struct Item {
     // so that its rows come out as O = 0, LSE = -inf through the usual path.
     const unsigned char *mrow[2];
     bool none[2];
+    int cnt[2];  // (block mask) tiles sub-tile t takes part in
 };
+
+// Kept tiles of one mask row within [lo_b, hi_b]: the highest, the lowest (-1
+// when none) and their count.  32 tiles at a time with independent loads, so a
+// long row costs a few memory latencies rather than one per tile.
+__device__ __forceinline__ void scan_mask_row(const unsigned char *mr, int lo_b, int hi_b, int &hi, int &lo,
+                                              int &cnt) {
+    hi = lo = -1;
+    cnt = 0;
+    for (int c0 = lo_b; c0 <= hi_b; c0 += 32) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int b = 0; b < 32; ++b)
+            if (c0 + b <= hi_b && __ldg(mr + c0 + b) != 0) bits |= 1u << b;
+        if (bits) {
+            if (lo < 0) lo = c0 + __ffs((int)bits) - 1;
+            hi = c0 + 31 - __clz((int)bits);
+            cnt += __popc(bits);
+        }
+    }
+}
 
 // The r-th item of this CTA: items are dealt out in rounds of gridDim.x in
 // snake order (CTA b takes r G + b in even rounds, r G + G - 1 - b in odd
@@ -220,6 +241,7 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
     g.act1 = g.row0 + kBlockM < p.Sq;
     g.mrow[0] = g.mrow[1] = nullptr;
     g.none[0] = g.none[1] = false;
+    g.cnt[0] = g.cnt[1] = 0;
     if constexpr (MASK) {
         {
             // each sub-tile's range shrinks to the tiles its mask row keeps
@@ -228,16 +250,13 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
             for (int t = 0; t < 2; ++t) {
                 if (t == 1 && !g.act1) break;
                 const unsigned char *mr = mh + (size_t)(2 * mblk + t) * (size_t)p.n_kv;
-                int hi = -1, lo = -1;
-                for (int j = g.jhi[t]; j >= g.jlo[t]; --j)
-                    if (mr[j]) {
-                        if (hi < 0) hi = j;
-                        lo = j;
-                    }
+                int hi, lo, cnt;
+                scan_mask_row(mr, g.jlo[t], g.jhi[t], hi, lo, cnt);
                 g.mrow[t] = mr;
                 g.none[t] = hi < 0;
                 g.jhi[t] = hi;
                 g.jlo[t] = lo;
+                g.cnt[t] = hi < 0 ? 1 : cnt;
             }
             // a sub-tile that keeps nothing rides along on the other's first tile
             // (tile 0 when neither keeps anything)
@@ -264,7 +283,7 @@ template <bool MASK>
 __device__ __forceinline__ bool takes_part(const Item &g, int t, int it) {
     if (it < g.first[t] || it > g.last[t]) return false;
     if constexpr (MASK) {
-        if (!g.none[t]) return g.mrow[t][g.J - it] != 0;
+        if (!g.none[t]) return __ldg(g.mrow[t] + (g.J - it)) != 0;
     }
     return true;
 }
@@ -286,20 +305,63 @@ __device__ __forceinline__ int next_live(const Item &g, int it) {
     }
 }
 
+// Block mask, MMA warp: which sub-tiles take part in 128 load-order tiles at a
+// time, gathered by the warp's 32 lanes with ballots, so that the issue loop
+// tests register bits instead of waiting on the mask's bytes in memory.  Every
+// lane runs the issue loop and takes the same branches, as the ballots need.
+struct PartBits {
+    int base;               // first load-order tile the words cover (a multiple of 128)
+    uint32_t w0[4], w1[4];  // bit b of word q: tile base + 32 q + b taken by sub-tile 0 / 1
+};
+template <bool MASK>
+__device__ __forceinline__ void part_fill(PartBits &pb, const Item &g, int base, int lane) {
+    pb.base = base;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int it = base + 32 * q + lane;
+        pb.w0[q] = __ballot_sync(0xffffffffu, it < g.N && takes_part<MASK>(g, 0, it));
+        pb.w1[q] = __ballot_sync(0xffffffffu, it < g.N && takes_part<MASK>(g, 1, it));
+    }
+}
+__device__ __forceinline__ uint32_t part_word(const uint32_t (&w)[4], int q) {
+    return q == 0 ? w[0] : q == 1 ? w[1] : q == 2 ? w[2] : w[3];
+}
+// bit 0: sub-tile 0 takes tile `it`, bit 1: sub-tile 1 does (it >= pb.base)
+template <bool MASK>
+__device__ __forceinline__ uint32_t part_of(PartBits &pb, const Item &g, int it, int lane) {
+    if (it - pb.base >= 128) part_fill<MASK>(pb, g, it & ~127, lane);
+    const int q = (it - pb.base) >> 5, b = (it - pb.base) & 31;
+    return ((part_word(pb.w0, q) >> b) & 1u) | (((part_word(pb.w1, q) >> b) & 1u) << 1);
+}
+// the next tile after `it` that some sub-tile takes (g.N if none)
+template <bool MASK>
+__device__ __forceinline__ int part_next(PartBits &pb, const Item &g, int it, int lane) {
+    for (int j = it + 1; j < g.N;) {
+        if (j - pb.base >= 128) part_fill<MASK>(pb, g, j & ~127, lane);
+        const int q = (j - pb.base) >> 5, b = (j - pb.base) & 31;
+        const uint32_t w = (part_word(pb.w0, q) | part_word(pb.w1, q)) >> b;
+        if (w) return j + __ffs((int)w) - 1;
+        j += 32 - b;
+    }
+    return g.N;
+}
+
 // WIN: a bounded key band (window_left >= 0 or window_right > 0).  Without it
 // (full or causal attention) only a sub-tile's first key tile can need a mask
 // and every row has an allowed key in it, which the code below exploits.
 // F8: Q, K, V are e4m3 with per-tensor scales (D = 128, no bounded band).
-// MASK (with WIN): a block mask keeps, per 128-row query block, a set of 128-key
+// MASK: a block mask keeps, per 128-row query block, a set of 128-key
 // tiles ("FlashAttention-2 — L3 Cross-Paper Synthesis", §5 item 4: causal block
 // skipping generalised into one sparse-block-skip mechanism).  An item's two
 // sub-tiles still share one K/V stream -- the tiles either of them keeps, in the
 // same descending order; tiles neither keeps are never loaded -- and each
 // sub-tile takes part only in its own tiles, so its S, P and P V run on those
-// alone.  A sub-tile that keeps nothing rides along on one loaded tile with
-// every key masked, which gives its rows O = 0 and LSE = -inf through the
-// banded path's handling of rows without a key.  (A separate instantiation: the
-// scan of the mask, even untaken, slowed the plain banded kernel by 11%.)
+// alone.  Causal and full attention keep the property that only a sub-tile's
+// first processed tile needs a mask and that every row has a key in it (the
+// tiles a row keeps lie at or below its diagonal tile).  A sub-tile that keeps
+// nothing rides along, unmasked, on one loaded tile and its rows are written as
+// O = 0 and LSE = -inf.  (Instantiations of their own: the scan of the mask,
+// even untaken, slowed the plain banded kernel by 11%.)
 template <int D, bool WIN, bool F8, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103a(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -581,14 +643,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qfp0 = (uint32_t)(qn0 / QB) & 1u;
                     qfp1 = (uint32_t)(qn1 / QB) & 1u;
                     const uint64_t dq0 = dqb + ((qb0 * C::QT_BYTES) >> 4), dq1 = dqb + ((qb1 * C::QT_BYTES) >> 4);
-                    for (int it = 0; ok && it < g.N; ++it) {
+                    PartBits pb;
+                    if constexpr (MASK) part_fill<MASK>(pb, g, 0, lane);
+                    // (block mask: tiles no sub-tile keeps are not loaded and skipped here)
+                    for (int it = 0, nxt; ok && it < g.N; it = nxt) {
+                        uint32_t pbits = 0;
                         if constexpr (MASK) {
-                            if (!tile_live<MASK>(g, it)) continue;  // not loaded: no sub-tile keeps it
+                            pbits = part_of<MASK>(pb, g, it, lane);
+                            nxt = part_next<MASK>(pb, g, it, lane);
+                        } else {
+                            nxt = it + 1;
                         }
                         ok = wait(B_K_FULL + sk, kph);
                         if (!ok) break;
-                        const bool p0 = takes_part<MASK>(g, 0, it);
-                        const bool p1 = takes_part<MASK>(g, 1, it);
+                        const bool p0 = MASK ? (pbits & 1u) != 0 : takes_part<MASK>(g, 0, it);
+                        const bool p1 = MASK ? (pbits & 2u) != 0 : takes_part<MASK>(g, 1, it);
                         if (p0) {
                             if (it == g.first[0]) ok = q_ready(0);
                             if (ok && ns0 > 0) ok = wait(B_S_FREE + 0, (uint32_t)(ns0 - 1) & 1u);
@@ -673,16 +742,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bool kready = false;  // K_FULL of key tile `it` already waited for
                         bool prev1 = false;   // (block mask) sub-tile 1 took part in the previous loaded tile
                         int prev_it = -1;     // (block mask) that tile
-                        for (int it = 0; ok && it < N; ++it) {
+                        PartBits pb;
+                        if constexpr (MASK) part_fill<MASK>(pb, g, 0, lane);
+                        // (block mask: tiles no sub-tile keeps are not loaded and skipped here)
+                        for (int it = 0, nxt; ok && it < N; it = nxt) {
+                            uint32_t pbits = 0;
                             if constexpr (MASK) {
-                                if (!tile_live<MASK>(g, it)) continue;  // not loaded: no sub-tile keeps it
+                                pbits = part_of<MASK>(pb, g, it, lane);
+                                nxt = part_next<MASK>(pb, g, it, lane);
+                            } else {
+                                nxt = it + 1;
                             }
                             if (!kready) ok = wait(B_K_FULL + sk, kph);
                             kready = false;
                             if (!ok) break;
                             tc_fence_after();
-                            const bool p0 = takes_part<MASK>(g, 0, it);
-                            const bool p1 = takes_part<MASK>(g, 1, it);
+                            const bool p0 = MASK ? (pbits & 1u) != 0 : takes_part<MASK>(g, 0, it);
+                            const bool p1 = MASK ? (pbits & 2u) != 0 : takes_part<MASK>(g, 1, it);
                             // sub-tile 1 took part in the previous tile, and whether that was its last
                             const bool pv1 = MASK ? prev1 : (it > first1 && it - 1 <= last1);
                             const bool pv1_last = MASK ? prev_it == last1 : it - 1 == last1;
@@ -715,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_commit(bar(B_K_EMPTY + sk));
                             // the next key tile's K is waited for here, so that P0 V and
                             // the next S0 issue back to back (S0 then waits on nothing)
-                            if (next_live<MASK>(g, it) < N) {
+                            if (nxt < N) {
                                 ok = wait(B_K_FULL + (sk + 1 == C::KST ? 0 : sk + 1), sk + 1 == C::KST ? kph ^ 1u : kph);
                                 if (!ok) break;
                                 kready = true;
@@ -776,8 +852,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_row = [&](const uint32_t (&o)[D / 32][32], float m, float l, int rg, int bh) {
             if (rg >= p.Sq) return;
             // 8-bit: O = descale_v * sum p' v / sum p' (the 2^kF8PShift cancels).
-            // A banded row with no allowed key (l = 0, O = 0): O = 0, LSE = -inf.
-            const float inv_l = (MASK && !(l > 0.f)) ? 0.f : (F8 ? p.o_scale : 1.f) / l;
+            // Block mask: a row with no allowed key (l = 0) is written as O = 0
+            // exactly and LSE = -inf.
+            const bool empty = MASK && !(l > 0.f);
+            const float inv_l = empty ? 0.f : (F8 ? p.o_scale : 1.f) / l;
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + ((size_t)bh * p.Sq + rg) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c)
@@ -786,11 +864,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(o[c][u * 8 + 2 * e]) * inv_l,
-                                           __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
+                        w[e] = empty ? 0u
+                                     : pack_bf16x2(__uint_as_float(o[c][u * 8 + 2 * e]) * inv_l,
+                                                   __uint_as_float(o[c][u * 8 + 2 * e + 1]) * inv_l);
                     dst[c * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            p.lse[(size_t)bh * p.Sq + rg] = (MASK && !(l > 0.f))
+            p.lse[(size_t)bh * p.Sq + rg] = empty
                                                 ? -INFINITY
                                                 : (m - (F8 ? kF8PShift : 0.f) + lg2_approx(l)) * 0.69314718055994531f;
         };
@@ -811,12 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visited from the highest (jt steps down to each in turn)
             const bool none = MASK && (t ? g.none[1] : g.none[0]);
             const unsigned char *mrow = (MASK && !none) ? (t ? g.mrow[1] : g.mrow[0]) : nullptr;
-            if constexpr (MASK) {
-                if (mrow) {
-                    n_t = 0;
-                    for (int j = my_jlo; j <= my_jhi; ++j) n_t += mrow[j] != 0;
-                }
-            }
+            if constexpr (MASK) n_t = t ? g.cnt[1] : g.cnt[0];
             int jt = my_jhi + 1;
             // allowed keys of this row: [k_lo, k_hi)
             const int k_lo = (p.wl >= 0) ? row_g - p.wl : 0;
@@ -844,14 +918,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (MASK) {
                     do {
                         --jt;
-                    } while (mrow && !mrow[jt]);
+                    } while (mrow && __ldg(mrow + jt) == 0);
                 }
                 const int col0 = (MASK ? jt : my_jhi - i) * C::BN;
-                const bool masked = WIN ? ((MASK && none) || col0 + C::BN > p.Sk ||
-                                           (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
-                                           (p.wl >= 0 && col0 < r_last - p.wl))
-                                        : (i == 0 && (p.wr >= 0 || (p.Sk % C::BN) != 0));
-                const int lim_lo = (MASK && none) ? 0 : k_lo - col0, lim_hi = (MASK && none) ? 0 : k_hi - col0;
+                // (A sub-tile whose mask row keeps nothing runs its one tile unmasked,
+                // on finite scores, and its rows are written as O = 0, LSE = -inf.)
+                const bool masked = (MASK && none)
+                                        ? false
+                                        : WIN ? (col0 + C::BN > p.Sk ||
+                                                 (p.wr >= 0 && col0 + C::BN - 1 > r_first + p.wr) ||
+                                                 (p.wl >= 0 && col0 < r_last - p.wl))
+                                              : (i == 0 && (p.wr >= 0 || (p.Sk % C::BN) != 0));
+                const int lim_lo = k_lo - col0, lim_hi = k_hi - col0;
                 if (F8 || masked || (WIN ? __any_sync(0xffffffffu, m_used == -INFINITY) : i == 0))
                     tmem_ld_wait2(s[2], s[3]);
                 if constexpr (C::P_SMEM) {
@@ -1154,6 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+            if (MASK && none) l_run = 0.f;  // no allowed key: O = 0, LSE = -inf
             if constexpr (C::SEPP) {  // epilogue deferred to the next item's first tile
                 pend = true;
                 pm = m_used;
@@ -1237,9 +1316,13 @@ static cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const FwdParams &p, int num_sms, cudaStream_t stream) {
     const bool win = p.wl >= 0 || p.wr > 0;
-    if (p.bmask)  // a block mask runs on the banded kernel's masking and empty-row handling
-        return D == 64 ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream)
-                       : launch_fwd_d<128, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream);
+    if (p.bmask) {  // block mask: on the banded kernel only where a band is given
+        if (D == 64)
+            return win ? launch_fwd_d<64, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream)
+                       : launch_fwd_d<64, false, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream);
+        return win ? launch_fwd_d<128, true, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream)
+                   : launch_fwd_d<128, false, false, true>(tm_q, tm_k, tm_v, p, num_sms, stream);
+    }
     if (D == 64)
         return win ? launch_fwd_d<64, true, false>(tm_q, tm_k, tm_v, p, num_sms, stream)
                    : launch_fwd_d<64, false, false>(tm_q, tm_k, tm_v, p, num_sms, stream);
