@@ -107,6 +107,20 @@ def test_blockmask_ragged_lengths(Sq, Sk):
 
 
 @pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("keep", [0.3, 0.9])
+def test_blockmask_long_key_rows(D, keep):
+    # 157 key tiles per row: the MMA warp's participation bits cover 128 load-order
+    # tiles at a time and are refilled past them, and a mask row is scanned in
+    # five 32-tile batches
+    B, H, Sq, Sk = 1, 2, 300, 20000
+    q, k, v = make_qkv(B, H, Sq, Sk, D, seed=950 + D + int(keep * 10))
+    mask = random_block_mask(B * H, _nb(Sq, 128), _nb(Sk, 128), keep, 95 + D)
+    mask[0, 0, 130:] = 0   # a row whose kept tiles end before the second window
+    mask[1, 1, :140] = 0   # a row whose kept tiles start in the second window
+    check(q, k, v, mask, (-1, -1), f"long rows D{D} keep{keep}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
 def test_blockmask_many_items(D):
     # 320 items of 256 query rows on at most one CTA per SM: persistent CTAs take
     # several items whose sub-tiles keep different, gapped sets of key tiles
