@@ -53,7 +53,7 @@ _SIGNATURES = {
     "fa_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
                            _vp]),
     "fa_fwd_blockmask": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
-                              _vp, _i, _vp]),
+                              _vp, _i, _i, _vp]),
     "fa_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp,
                             ctypes.c_size_t, _vp]),
     "fa_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
@@ -137,11 +137,12 @@ def fa_fwd_window_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: i
 
 def fa_fwd_blockmask_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
                          H: int, Sq: int, Sk: int, D: int, scale: float, window_left: int,
-                         window_right: int, mask_ptr: int, mask_heads: int, stream_ptr: int) -> int:
+                         window_right: int, mask_ptr: int, mask_heads: int, pair_stride: int,
+                         stream_ptr: int) -> int:
     """The block-mask C call with raw device pointers; returns the status code."""
     return lib().fa_fwd_blockmask(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Sq, Sk, D, float(scale),
                                   int(window_left), int(window_right), mask_ptr, int(mask_heads),
-                                  stream_ptr)
+                                  int(pair_stride), stream_ptr)
 
 
 def _prepare(q, k, v, o, lse):
@@ -200,11 +201,13 @@ def fa_fwd_window(q, k, v, window_left: int, window_right: int, o=None, lse=None
 
 
 def fa_fwd_blockmask(q, k, v, block_mask, window_left: int = -1, window_right: int = -1, o=None,
-                     lse=None, scale: float | None = None, stream=None):
+                     lse=None, scale: float | None = None, pair_stride: int = 1, stream=None):
     """Attention over the key blocks ``block_mask`` keeps (uint8 or bool CUDA tensor
     ``[mask_heads, ceil(Sq/128), ceil(Sk/128)]``, ``mask_heads`` 1 or B*H; nonzero
     keeps a 128-row x 128-key block), within the band of fa_fwd_window.  Rows with
-    no allowed key get O = 0, LSE = -inf.  Same tensors and return value as fa_fwd."""
+    no allowed key get O = 0, LSE = -inf.  ``pair_stride``: query blocks a and
+    a + pair_stride are computed together (a hint; the stride of a dilated
+    pattern suits it).  Same tensors and return value as fa_fwd."""
     import torch
 
     o, lse, B, H, Sq, Sk, D = _prepare(q, k, v, o, lse)
@@ -217,7 +220,7 @@ def fa_fwd_blockmask(q, k, v, block_mask, window_left: int = -1, window_right: i
         raise ValueError(f"block_mask must be a contiguous CUDA uint8/bool tensor [mask_heads, {n_qb}, {n_kb}]")
     st = fa_fwd_blockmask_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               B, H, Sq, Sk, D, scale, window_left, window_right,
-                              block_mask.data_ptr(), block_mask.shape[0], _stream_ptr(stream))
+                              block_mask.data_ptr(), block_mask.shape[0], pair_stride, _stream_ptr(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_blockmask")
     return o, lse

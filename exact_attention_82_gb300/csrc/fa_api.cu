@@ -89,7 +89,7 @@ extern "C" const char *fa_strerror(int status) {
         case FA_ERR_ALIAS: s = "an output buffer overlaps an input or the other output"; break;
         case FA_ERR_BAD_WINDOW: s = "window bounds must be >= -1, and a bounded window needs Sq == Sk"; break;
         case FA_ERR_WORKSPACE: s = "workspace missing, not 16-byte aligned, or smaller than required"; break;
-        case FA_ERR_BAD_MASK: s = "mask_heads must be 1 or B * H"; break;
+        case FA_ERR_BAD_MASK: s = "mask_heads must be 1 or B * H, and pair_stride >= 1"; break;
         case FA_ERR_SCRATCH_LIMIT:
             s = "needs more scratch than the built-in 16 MiB buffer of fa_fwd_splitkv_noalloc holds; "
                 "pass a workspace to fa_fwd_splitkv instead";
@@ -144,10 +144,15 @@ static int check_fwd(const void *q, const void *k, const void *v, const void *o,
 static int launch_checked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Sq,
                           int Sk, int D, float scale, int wl, int wr, void *stream,
                           unsigned long long timeout_ns = kWaitLimitNs, const unsigned char *bmask = nullptr,
-                          long long bmask_hstride = 0) {
+                          long long bmask_hstride = 0, int pair_stride = 1) {
     if (!get_encoder()) return fail_cuda(cudaErrorNotSupported);
     const long long BH = (long long)B * H;
-    const long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
+    long long n_mblk = (Sq + fa::kCtaRows - 1) / fa::kCtaRows;
+    if (bmask) {  // items of one head when query blocks a and a + pair_stride are paired
+        const long long n_qb = (Sq + fa::kBlockM - 1) / fa::kBlockM, s = pair_stride;
+        const long long whole = n_qb / (2 * s);
+        n_mblk = whole * s + (n_qb - 2 * s * whole + 1) / 2;
+    }
     CUtensorMap tm_q, tm_k, tm_v;
     if (!encode_bhsd(&tm_q, q, D, Sq, BH, fa::kBlockM) || !encode_bhsd(&tm_k, k, D, Sk, BH, fa::kBlockN) ||
         !encode_bhsd(&tm_v, v, D, Sk, BH, fa::kBlockN))
@@ -169,6 +174,7 @@ static int launch_checked(const void *q, const void *k, const void *v, void *o, 
     p.timeout_ns = timeout_ns;
     p.bmask = bmask;
     p.bmask_hstride = bmask_hstride;
+    p.pair_stride = pair_stride;
     const cudaError_t e = fa::launch_fwd(D, tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;
@@ -195,7 +201,7 @@ extern "C" int fa_fwd_window(const void *q, const void *k, const void *v, void *
 
 extern "C" int fa_fwd_blockmask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                                 int Sq, int Sk, int D, float scale, int window_left, int window_right,
-                                const unsigned char *block_mask, int mask_heads, void *stream) {
+                                const unsigned char *block_mask, int mask_heads, int pair_stride, void *stream) {
     const int st = check_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale);
     if (st != FA_OK) return st;
     if (!block_mask) return FA_ERR_NULLPTR;
@@ -203,13 +209,16 @@ extern "C" int fa_fwd_blockmask(const void *q, const void *k, const void *v, voi
     if ((window_left >= 0 || window_right >= 0) && Sq != Sk) return FA_ERR_BAD_WINDOW;
     const long long BH = (long long)B * H;
     if (mask_heads != 1 && (long long)mask_heads != BH) return FA_ERR_BAD_MASK;
+    if (pair_stride < 1) return FA_ERR_BAD_MASK;
     const long long n_qb = (Sq + fa::kBlockM - 1) / fa::kBlockM, n_kb = (Sk + fa::kBlockN - 1) / fa::kBlockN;
     const size_t mask_bytes = (size_t)mask_heads * (size_t)(n_qb * n_kb);
     const size_t o_bytes = (size_t)BH * Sq * D * 2, lse_bytes = (size_t)BH * Sq * 4;
     if (overlaps(block_mask, mask_bytes, o, o_bytes) || overlaps(block_mask, mask_bytes, lse, lse_bytes))
         return FA_ERR_ALIAS;
+    // a stride of n_qb or more pairs nothing apart: every block with its neighbour
+    const int stride = (int)std::min<long long>(pair_stride, n_qb);
     return launch_checked(q, k, v, o, lse, B, H, Sq, Sk, D, scale, window_left, window_right, stream, kWaitLimitNs,
-                          block_mask, mask_heads == 1 ? 0 : n_qb * n_kb);
+                          block_mask, mask_heads == 1 ? 0 : n_qb * n_kb, stride);
 }
 
 extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
@@ -258,6 +267,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, 
     p.timeout_ns = kWaitLimitNs;
     p.bmask = nullptr;
     p.bmask_hstride = 0;
+    p.pair_stride = 1;
     const cudaError_t e = fa::launch_fwd_fp8(tm_q, tm_k, tm_v, p, sm_count(), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return FA_OK;

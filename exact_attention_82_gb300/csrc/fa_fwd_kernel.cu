@@ -176,6 +176,7 @@ __host__ __device__ constexpr int query_buffers(int D, bool F8) { return (D == 6
 // down to J - N + 1; sub-tile t takes part in load-order tiles first_t..last_t.
 struct Item {
     int bh, row0;
+    int qrow[2];  // first query row of each sub-tile (row0 and row0 + 128 unless paired apart)
     bool act1;  // sub-tile 1 has rows (sub-tile 0 always has)
     int jhi[2], jlo[2];
     int J, N;
@@ -231,14 +232,32 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
     }
     const int mblk = p.causal ? (p.n_mblk - 1 - mi) : mi;
     g.row0 = mblk * kCtaRows;
+    g.qrow[0] = g.row0;
+    g.qrow[1] = g.row0 + kBlockM;
+    if constexpr (MASK) {
+        // Block mask: query blocks a and a + s (s = pair_stride) share an item, in
+        // groups of 2 s blocks; the blocks after the last whole group pair up
+        // with their neighbours.  With s = 1 this is the usual pairing.
+        const int s = p.pair_stride, whole = (p.Sq + kBlockM - 1) / kBlockM / (2 * s);
+        int qb0, qb1;
+        if (mblk < whole * s) {
+            qb0 = 2 * s * (mblk / s) + mblk % s;
+            qb1 = qb0 + s;
+        } else {
+            qb0 = 2 * s * whole + 2 * (mblk - whole * s);
+            qb1 = qb0 + 1;
+        }
+        g.qrow[0] = qb0 * kBlockM;
+        g.qrow[1] = qb1 * kBlockM;
+    }
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int r_first = g.row0 + t * kBlockM, r_last = r_first + kBlockM - 1;
+        const int r_first = g.qrow[t], r_last = r_first + kBlockM - 1;
         g.jhi[t] = p.n_kv - 1;
         if (p.wr >= 0) g.jhi[t] = min(g.jhi[t], (r_last + p.wr) / kBlockN);
         g.jlo[t] = (WIN && p.wl >= 0) ? max(0, (r_first - p.wl) / kBlockN) : 0;
     }
-    g.act1 = g.row0 + kBlockM < p.Sq;
+    g.act1 = g.qrow[1] < p.Sq;
     g.mrow[0] = g.mrow[1] = nullptr;
     g.none[0] = g.none[1] = false;
     g.cnt[0] = g.cnt[1] = 0;
@@ -249,7 +268,7 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (t == 1 && !g.act1) break;
-                const unsigned char *mr = mh + (size_t)(2 * mblk + t) * (size_t)p.n_kv;
+                const unsigned char *mr = mh + (size_t)(g.qrow[t] / kBlockM) * (size_t)p.n_kv;
                 int hi, lo, cnt;
                 scan_mask_row(mr, g.jlo[t], g.jhi[t], hi, lo, cnt);
                 g.mrow[t] = mr;
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(B_Q_FULL + slot), C::QT_BYTES);
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_3d(sQ + slot * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS,
-                                g.row0 + t * C::BM, g.bh, bar(B_Q_FULL + slot), pol_q);
+                                t ? g.qrow[1] : g.qrow[0], g.bh, bar(B_Q_FULL + slot), pol_q);
                 ++qr;
                 return true;
             };
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(B_Q_FULL + qb), C::QT_BYTES);
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_3d(sQ + qb * C::QT_BYTES + c * C::CHUNK, &tm_q, c * C::CH_ELEMS,
-                                    g.row0 + t * C::BM, g.bh, bar(B_Q_FULL + qb), pol_q);
+                                    t ? g.qrow[1] : g.qrow[0], g.bh, bar(B_Q_FULL + qb), pol_q);
                     ++qn;
                     return true;
                 };
@@ -883,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             g = item_at<WIN, MASK>(p, k);
             if (t == 1 && !g.act1) continue;
             const int my_jhi = t ? g.jhi[1] : g.jhi[0], my_jlo = t ? g.jlo[1] : g.jlo[0];
-            const int r_first = g.row0 + t * C::BM, r_last = r_first + C::BM - 1;
+            const int r_first = t ? g.qrow[1] : g.qrow[0], r_last = r_first + C::BM - 1;
             const int row_g = r_first + row;
             int n_t = my_jhi - my_jlo + 1;
             // block mask: the tiles of [my_jlo, my_jhi] this sub-tile's row keeps,

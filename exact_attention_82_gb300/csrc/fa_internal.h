@@ -30,6 +30,10 @@ struct FwdParams {
     // the head for bmask_hstride = n_qb * n_kv and 0 for bmask_hstride = 0.
     const unsigned char *bmask;
     long long bmask_hstride;
+    // Block mask: query blocks a and a + pair_stride share a work item (and its
+    // K/V loads), in groups of 2 * pair_stride blocks; n_mblk then counts the
+    // items of one head.  1 elsewhere.
+    int pair_stride;
 };
 
 // Split-KV (decode) launch: partials per (head, split), then a merge.

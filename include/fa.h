@@ -54,7 +54,7 @@ typedef enum {
     FA_ERR_BAD_WINDOW = -10,        /* window bound below -1, or band with Sq != Sk  */
     FA_ERR_WORKSPACE = -11,         /* workspace missing, misaligned or too small    */
     FA_ERR_SCRATCH_LIMIT = -12,     /* more scratch than the built-in buffer holds   */
-    FA_ERR_BAD_MASK = -13           /* block mask heads other than 1 or B * H        */
+    FA_ERR_BAD_MASK = -13           /* mask heads not 1 or B * H, or pair stride < 1 */
 } fa_status;
 
 /*
@@ -119,18 +119,24 @@ int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *l
  *               DEVICE pointer, read by the kernel (must stay valid until the
  *               stream passes it), any alignment, must not overlap O or LSE
  *   mask_heads  1 or B * H
+ *   pair_stride >= 1, a scheduling hint that does not change the result: query
+ *               blocks a and a + pair_stride are computed together (in groups
+ *               of 2 * pair_stride blocks; the last blocks with their
+ *               neighbours) and share the loads of the key blocks either keeps.
+ *               1 suits masks whose neighbouring rows keep like blocks (bands,
+ *               random masks); a dilated pattern with stride r wants r.
  * Other arguments, layout, ownership and outputs are those of fa_fwd_window.
  * A query row with no allowed key (its block row keeps nothing, or the band
  * leaves nothing of what it keeps) gets O = 0 and LSE = -inf.
  * Errors: those of fa_fwd_window, plus FA_ERR_NULLPTR for a null mask,
- * FA_ERR_BAD_MASK for mask_heads other than 1 or B * H, and FA_ERR_ALIAS when
+ * FA_ERR_BAD_MASK for mask_heads other than 1 or B * H or pair_stride < 1, and FA_ERR_ALIAS when
  * the mask overlaps O or LSE.  With every block kept it equals fa_fwd_window.
  */
 #define FA_BLOCK_M 128
 #define FA_BLOCK_N 128
 int fa_fwd_blockmask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                      int Sq, int Sk, int D, float scale, int window_left, int window_right,
-                     const unsigned char *block_mask, int mask_heads, void *stream);
+                     const unsigned char *block_mask, int mask_heads, int pair_stride, void *stream);
 
 /*
  * fa_fwd_fp8 -- attention forward with 8-bit (e4m3) Q, K, V and per-tensor

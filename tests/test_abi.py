@@ -131,14 +131,15 @@ def test_window_argument_checks():
         fa.FA_ERR_UNSUPPORTED_D
 
 
-def mcall(mask=1 << 42, heads=1, B=1, H=1, Sq=300, Sk=300, wl=-1, wr=-1, o=A4, lse=A5, D=64):
-    return fa.fa_fwd_blockmask_raw(A, A2, A3, o, lse, B, H, Sq, Sk, D, 0.125, wl, wr, mask, heads, 0)
+def mcall(mask=1 << 42, heads=1, B=1, H=1, Sq=300, Sk=300, wl=-1, wr=-1, o=A4, lse=A5, D=64, stride=1):
+    return fa.fa_fwd_blockmask_raw(A, A2, A3, o, lse, B, H, Sq, Sk, D, 0.125, wl, wr, mask, heads, stride, 0)
 
 
 def test_blockmask_argument_checks():
     assert mcall(mask=0) == fa.FA_ERR_NULLPTR
     assert mcall(heads=2, B=1, H=3) == fa.FA_ERR_BAD_MASK
     assert mcall(heads=0) == fa.FA_ERR_BAD_MASK
+    assert mcall(stride=0) == fa.FA_ERR_BAD_MASK
     assert mcall(wl=-2) == fa.FA_ERR_BAD_WINDOW
     assert mcall(wl=16, wr=0, Sq=128, Sk=256) == fa.FA_ERR_BAD_WINDOW
     assert mcall(D=96) == fa.FA_ERR_UNSUPPORTED_D
@@ -153,6 +154,7 @@ def test_blockmask_argument_checks():
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path only")
 def test_blockmask_valid_call_without_gpu_reports_cuda_error():
     assert mcall(heads=3, B=1, H=3) == fa.FA_ERR_CUDA
+    assert mcall(stride=1 << 30) == fa.FA_ERR_CUDA
     assert mcall(mask=A4 - 9) == fa.FA_ERR_CUDA  # 9 bytes of mask end right before O
 
 

@@ -33,10 +33,11 @@ def _nb(S, b):
     return -(-S // b)
 
 
-def run_mask(q, k, v, mask, window=(-1, -1), scale=None):
+def run_mask(q, k, v, mask, window=(-1, -1), scale=None, pair_stride=1):
     D = q.shape[3]
     scale = D ** -0.5 if scale is None else scale
-    o, lse = fa.fa_fwd_blockmask(q.cuda(), k.cuda(), v.cuda(), mask.cuda(), window[0], window[1], scale=scale)
+    o, lse = fa.fa_fwd_blockmask(q.cuda(), k.cuda(), v.cuda(), mask.cuda(), window[0], window[1], scale=scale,
+                                 pair_stride=pair_stride)
     torch.cuda.synchronize()
     return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
 
@@ -59,10 +60,10 @@ def compare_masked(og, lg, ro, rl, what):
     assert dl.max() <= TOL_LSE, msg
 
 
-def check(q, k, v, mask, window, what, scale=None):
+def check(q, k, v, mask, window, what, scale=None, pair_stride=1):
     D = q.shape[3]
     scale = D ** -0.5 if scale is None else scale
-    og, lg = run_mask(q, k, v, mask, window, scale)
+    og, lg = run_mask(q, k, v, mask, window, scale, pair_stride)
     ro, rl = oracle.attn_fwd_blockmask(*(bf16_bits(t) for t in (q, k, v)), scale, mask.numpy(),
                                        window=window, block=BLK)
     compare_masked(og, lg, ro, rl, what)
@@ -118,6 +119,36 @@ def test_blockmask_long_key_rows(D, keep):
     mask[0, 0, 130:] = 0   # a row whose kept tiles end before the second window
     mask[1, 1, :140] = 0   # a row whose kept tiles start in the second window
     check(q, k, v, mask, (-1, -1), f"long rows D{D} keep{keep}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("stride,causal", [(2, True), (3, False), (4, True)])
+def test_dilated_with_matching_pair_stride(D, stride, causal):
+    # query blocks a and a + stride share an item: for a dilated pattern they keep
+    # the same key blocks (causal: one more for the second); 11 query blocks leave
+    # a tail of blocks paired with their neighbours
+    B, H, S = 2, 2, 1400
+    q, k, v = make_qkv(B, H, S, S, D, seed=1000 + D + stride)
+    n = _nb(S, 128)
+    mask = dilated_block_mask(n, n, stride, causal=causal)
+    check(q, k, v, mask, (-1, 0) if causal else (-1, -1), f"dilated {stride} D{D}", pair_stride=stride)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_pair_stride_changes_nothing_but_the_schedule(D):
+    # every stride (1 .. beyond the block count) gives bitwise the same O and LSE,
+    # for a random per-head mask with a band and query blocks that keep nothing
+    B, H, S = 1, 3, 1300
+    q, k, v = make_qkv(B, H, S, S, D, seed=1100 + D)
+    n = _nb(S, 128)
+    mask = random_block_mask(B * H, n, n, 0.4, 110 + D)
+    mask[1, 2] = 0
+    for window in [(-1, -1), (500, 0)]:
+        ref = run_mask(q, k, v, mask, window, pair_stride=1)
+        for s in (2, 3, 5, 7, 100):
+            got = run_mask(q, k, v, mask, window, pair_stride=s)
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), (window, s)
+    check(q, k, v, mask, (500, 0), f"stride 3 band D{D}", pair_stride=3)
 
 
 @pytest.mark.parametrize("D", [64, 128])
