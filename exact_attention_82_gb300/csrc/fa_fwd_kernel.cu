@@ -181,8 +181,8 @@ struct Item {
     int jhi[2], jlo[2];
     int J, N;
     int first[2], last[2];
-    // Block mask (banded kernel): mrow[t] is sub-tile t's row of the mask (null:
-    // no mask, every tile of its range taken).  A sub-tile whose row keeps no
+    // Block mask: mrow[t] is sub-tile t's row of the mask (null: every tile of
+    // its range [jlo, jhi] taken -- no mask, or a row that keeps a contiguous run).  A sub-tile whose row keeps no
     // tile of its range takes part in one tile with every key masked ("none"),
     // so that its rows come out as O = 0, LSE = -inf through the usual path.
     const unsigned char *mrow[2];
@@ -271,7 +271,9 @@ __device__ __forceinline__ Item item_at(const FwdParams &p, int k) {
                 const unsigned char *mr = mh + (size_t)(g.qrow[t] / kBlockM) * (size_t)p.n_kv;
                 int hi, lo, cnt;
                 scan_mask_row(mr, g.jlo[t], g.jhi[t], hi, lo, cnt);
-                g.mrow[t] = mr;
+                // a row that keeps every tile from its lowest to its highest is a plain
+                // range: no per-tile lookups for it
+                g.mrow[t] = (hi >= 0 && cnt == hi - lo + 1) ? nullptr : mr;
                 g.none[t] = hi < 0;
                 g.jhi[t] = hi;
                 g.jlo[t] = lo;
@@ -302,7 +304,7 @@ template <bool MASK>
 __device__ __forceinline__ bool takes_part(const Item &g, int t, int it) {
     if (it < g.first[t] || it > g.last[t]) return false;
     if constexpr (MASK) {
-        if (!g.none[t]) return __ldg(g.mrow[t] + (g.J - it)) != 0;
+        if (g.mrow[t] && !g.none[t]) return __ldg(g.mrow[t] + (g.J - it)) != 0;
     }
     return true;
 }
