@@ -250,6 +250,9 @@ def run_path(fa, w, q, k, v, o, lse, ws, stream):
         fa.fa_fwd_splitkv(q, k, v, o=o, lse=lse, scale=w.scale, workspace=ws, stream=stream)
     elif w.path == "fp8":
         fa.fa_fwd_fp8(q, k, v, *ws, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+    elif w.path == "blockmask":
+        fa.fa_fwd_blockmask(q, k, v, ws, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
+                            pair_stride=w.dilation, stream=stream)
     elif w.window_left >= 0:
         fa.fa_fwd_window(q, k, v, w.window[0], w.window[1], o=o, lse=lse, scale=w.scale,
                          stream=stream)
@@ -276,6 +279,8 @@ def make_workspace(fa, w, q, k, v, dev, descales=None):
 
     if w.path == "fp8":
         return descales
+    if w.path == "blockmask":  # the pattern: a fixed input, on the device before timing
+        return w.block_mask.to(dev)
     if w.path == "splitkv":
         return torch.empty(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, w.D),
                            dtype=torch.uint8, device=dev)
@@ -579,7 +584,25 @@ def _oracle_inputs(q, k, v, descales):
 
 def cpu_baseline(w, q, k, v, target_s, descales=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the
-    same workload: whole heads, grown until about `target_s` seconds."""
+    same workload: whole heads, grown until about `target_s` seconds (block-mask
+    path: whole query blocks from the middle of as many heads as there are cores)."""
+    if w.path == "blockmask":
+        from exact_attention_82_gb300.inputs import BLOCK
+
+        cores = _host_cores()
+        BH = w.B * w.H
+        rows = min(w.Sq, 8 * BLOCK)  # (the oracle holds rows x Sk fp64 arrays per head)
+        r0 = max(0, (w.Sq // 2 - rows // 2) // BLOCK * BLOCK)
+        nh = min(BH, cores)
+        dt, fl = _RowSampler(w, q, k, v, None, nh).run(r0, rows)
+        if dt < target_s / 4 and nh < BH:
+            nh = min(BH, max(nh + 1, int(nh * target_s / max(dt, 1e-3) * 0.8)))
+            dt, fl = _RowSampler(w, q, k, v, None, nh).run(r0, rows)
+        return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle", "seconds": round(dt, 2),
+                "sample": f"query rows {r0}..{min(w.Sq, r0 + rows) - 1} of {nh} of {BH} (batch,head) pairs of "
+                          f"{w.name}, with every key; fp64 numpy block-mask oracle forward with S and P "
+                          f"materialised (numpy's matmul threads)"}
     qb, kb, vb = _oracle_inputs(q, k, v, descales)
     gb = _dout_bits(w) if w.path == "bwd" else None
     cores = _host_cores()
@@ -620,6 +643,7 @@ class _RowSampler:
 
         ds = descales if descales is not None else (None, None, None)
         self.q, self.k, self.v = (heads(t, d) for t, d in zip((q, k, v), ds))
+        self.mask = w.block_mask.numpy() if w.path == "blockmask" else None
         self.g = None
         if w.path == "bwd":
             from exact_attention_82_gb300.inputs import SEED_BASE, make_qkv
@@ -631,6 +655,8 @@ class _RowSampler:
         import oracle
 
         w = self.w
+        if w.path == "blockmask":
+            return self._run_blockmask(r0, rows)
         wl, wr = w.window
         r1 = min(w.Sq, r0 + rows)
         k0 = max(0, r0 - wl) if wl >= 0 else 0
@@ -649,6 +675,32 @@ class _RowSampler:
             oracle.attn_bwd(qa, ka, va, self.g[None, :, r0:r1], w.scale, False, win, nthreads=_host_cores())
         else:
             oracle.attn_fwd(qa, ka, va, w.scale, False, win, nthreads=_host_cores())
+        return time.perf_counter() - t0, flops
+
+
+    def _run_blockmask(self, r0, rows):
+        """Whole query blocks covering rows r0 .. r0 + rows - 1, against every key:
+        the block-mask oracle on those rows, with the causal bound shifted to the
+        slice's row indices."""
+        import oracle
+        from exact_attention_82_gb300.inputs import BLOCK
+
+        w = self.w
+        a0 = r0 // BLOCK
+        a1 = -(-min(w.Sq, r0 + rows) // BLOCK)
+        rb0, rb1 = a0 * BLOCK, min(w.Sq, a1 * BLOCK)
+        kept = self.mask[0] != 0
+        i = np.arange(rb0, rb1)[:, None]
+        j = np.arange(w.Sk)[None, :]
+        allowed = kept[i // BLOCK, j // BLOCK]
+        if w.causal:
+            allowed &= j <= i
+        flops = 4.0 * w.D * float(allowed.sum()) * self.nh
+        win = (-1, rb0) if w.causal else (-1, -1)
+        qa = self.q[None, :, rb0:rb1]
+        t0 = time.perf_counter()
+        oracle.attn_fwd_blockmask(qa, self.k[None], self.v[None], w.scale, self.mask[:, a0:a1],
+                                  window=win, block=(BLOCK, BLOCK))
         return time.perf_counter() - t0, flops
 
 
@@ -696,6 +748,11 @@ def run_reference(args):
               f"step (of {w.Sq} rows x {BH} heads), rows advancing per step, with exactly the "
               f"keys they may see; fp64 C oracle {what}, a thread per head, S and P "
               f"materialised; {REFERENCE_BUDGET_S:.0f} s budget for the whole run")
+    if w.path == "blockmask":
+        sample = (f"whole 128-row query blocks covering {rows} rows of each of {nh} (batch, head) pairs "
+                  f"of {w.name} per step, rows advancing per step, with every key; fp64 numpy "
+                  f"block-mask oracle forward, S and P materialised; {REFERENCE_BUDGET_S:.0f} s budget "
+                  f"for the whole run")
     return {
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,

@@ -38,7 +38,9 @@ class Workload:
     causal: bool
     q_mult: float = 1.0
     window_left: int = -1   # keys i - window_left .. i (+ window_right); -1: unbounded
-    path: str = "fwd"       # "fwd", "splitkv" (decode, key-split), "bwd" (gradients), "fp8"
+    path: str = "fwd"       # "fwd", "splitkv" (decode, key-split), "bwd" (gradients), "fp8",
+                            # "blockmask" (a dilated block pattern)
+    dilation: int = 0       # "blockmask": the pattern's stride (also the pairing stride)
 
     @property
     def window(self):
@@ -50,9 +52,18 @@ class Workload:
         return 1.0 / math.sqrt(self.D)
 
     @property
+    def block_mask(self) -> torch.Tensor:
+        """The "blockmask" path's uint8 [1, ceil(Sq/128), ceil(Sk/128)] mask."""
+        return dilated_block_mask(-(-self.Sq // BLOCK), -(-self.Sk // BLOCK), self.dilation, self.causal)
+
+    @property
     def flops(self) -> float:
         """Matmul FLOPs 4*B*H*Sq*Sk*D, halved when causal (the metric's rule); with a
-        bounded window, 4*B*H*D times the exact number of allowed (query, key) pairs."""
+        bounded window or a block mask, 4*B*H*D times the exact number of allowed
+        (query, key) pairs."""
+        if self.path == "blockmask":
+            return 4.0 * self.B * self.H * self.D * float(block_mask_pairs(self.block_mask[0].numpy(), self.Sq,
+                                                                           self.Sk, self.causal))
         if self.window_left >= 0:
             i = np.arange(self.Sq)
             hi = np.minimum(self.Sk - 1, i if self.causal else self.Sk - 1)
@@ -67,8 +78,9 @@ class Workload:
     def hbm_bytes(self) -> float:
         """Algorithmic HBM bytes: Q, K, V read once, O and LSE written once."""
         eb = 1 if self.path == "fp8" else 2
+        mask = -(-self.Sq // BLOCK) * -(-self.Sk // BLOCK) if self.path == "blockmask" else 0
         return float(self.B * self.H * (eb * (self.Sq + 2 * self.Sk) * self.D + 2 * self.Sq * self.D
-                                        + 4 * self.Sq))
+                                        + 4 * self.Sq) + mask)
 
     def describe(self) -> str:
         c = "causal" if self.causal else "non-causal"
@@ -78,6 +90,9 @@ class Workload:
             c += ", split-KV decode"
         if self.path == "bwd":
             c += ", backward (dQ, dK, dV)"
+        if self.path == "blockmask":
+            c += (f", dilated block mask (128 x 128 blocks; key block c kept for query block a iff "
+                  f"a - c is a multiple of {self.dilation}), pair_stride {self.dilation}")
         extra = f", Q x{self.q_mult:g}" if self.q_mult != 1.0 else ""
         dt = "e4m3 (per-tensor scale)" if self.path == "fp8" else "bf16"
         return (f"B={self.B},H={self.H},Sq={self.Sq},Sk={self.Sk},D={self.D}, {dt} N(0,1)"
@@ -101,7 +116,10 @@ WORKLOADS = [
     # 8-bit (e4m3) Q, K, V with per-tensor scales, the headline shape and causal
     Workload("b8h16s2048d128_fp8", 8, 16, 2048, 2048, 128, False, path="fp8"),
     Workload("b4h16s4096d128_causal_fp8", 4, 16, 4096, 4096, 128, True, path="fp8"),
+    # a dilated causal block pattern (every 2nd 128-key block): a quarter of the pairs
+    Workload("b2h32s16384d128_dilated2_causal", 2, 32, 16384, 16384, 128, True, path="blockmask", dilation=2),
 ]
+BLOCK = 128  # rows and keys per block of a block mask
 
 
 def make_qkv(B: int, H: int, Sq: int, Sk: int, D: int, seed: int, q_mult: float = 1.0):
@@ -184,3 +202,18 @@ def dilated_block_mask(n_qb: int, n_kb: int, stride: int, causal: bool = False) 
     if causal:
         keep &= c <= a
     return keep.to(torch.uint8).unsqueeze(0).contiguous()
+
+
+def block_mask_pairs(mask, Sq: int, Sk: int, causal: bool) -> int:
+    """Allowed (query, key) pairs of a [n_qb, n_kb] block mask (FLOP accounting):
+    a kept block contributes its rows x keys, a causal diagonal block its lower
+    triangle (Sq == Sk), a block above the diagonal nothing."""
+    n = 0
+    for a in range(mask.shape[0]):
+        rq = min(BLOCK, Sq - BLOCK * a)
+        for c in range(mask.shape[1]):
+            if not mask[a, c] or (causal and c > a):
+                continue
+            rk = min(BLOCK, Sk - BLOCK * c)
+            n += rq * (rq + 1) // 2 if (causal and c == a) else rq * rk
+    return n

@@ -126,3 +126,45 @@ def test_reference_sampler_rows_equal_full_computation(monkeypatch, causal, wl, 
     pairs = sum(1 for i in range(r0, r1) for j in range(S)
                 if not (causal and j > i) and not (wl >= 0 and j < i - wl))
     assert flops == 4.0 * D * pairs * H
+
+
+@pytest.mark.parametrize("S,stride,causal", [(300, 2, True), (520, 3, False), (128, 2, True), (1, 2, False)])
+def test_blockmask_flops_count_allowed_pairs(S, stride, causal):
+    """The block-mask workloads' FLOPs: 4*B*H*D times the allowed pairs, counted here
+    by brute force over every (query, key) pair of the pattern."""
+    from exact_attention_82_gb300.inputs import dilated_block_mask
+
+    w = Workload("t", 2, 3, S, S, 16, causal, path="blockmask", dilation=stride)
+    m = dilated_block_mask(-(-S // 128), -(-S // 128), stride, causal)[0].numpy()
+    pairs = sum(1 for i in range(S) for j in range(S) if m[i // 128, j // 128] and not (causal and j > i))
+    assert w.flops == 4.0 * 2 * 3 * 16 * pairs
+    assert w.hbm_bytes == 2 * 3 * (2 * 3 * S * 16 + 2 * S * 16 + 4 * S) + m.size
+
+
+@pytest.mark.parametrize("causal,r0,rows", [(True, 130, 100), (False, 0, 128), (True, 0, 300)])
+def test_reference_sampler_blockmask_rows_equal_full_computation(monkeypatch, causal, r0, rows):
+    """For a block mask the reference arm evaluates whole query blocks against
+    every key, the causal bound shifted to the slice; its output must be those rows
+    of the full computation, and its FLOP count theirs."""
+    B, H, S, D = 1, 2, 300, 16
+    w = Workload("t", B, H, S, S, D, causal, path="blockmask", dilation=2)
+    q, k, v = make_qkv(B, H, S, S, D, seed=32)
+    sampler = bench._RowSampler(w, q, k, v, None, nh=H)
+    got = {}
+    real = oracle.attn_fwd_blockmask
+
+    def spy(*a, **kw):
+        got["out"] = real(*a, **kw)
+        return got["out"]
+
+    monkeypatch.setattr(oracle, "attn_fwd_blockmask", spy)
+    _, flops = sampler.run(r0, rows)
+    o_full, l_full = real(sampler.q[None], sampler.k[None], sampler.v[None], w.scale, w.block_mask.numpy(),
+                          window=w.window, block=(128, 128))
+    rb0, rb1 = (r0 // 128) * 128, min(S, -(-(r0 + rows) // 128) * 128)
+    o_s, l_s = got["out"]
+    np.testing.assert_allclose(o_s[0], o_full[0][:, rb0:rb1], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l_s[0], l_full[0][:, rb0:rb1], rtol=1e-12, atol=1e-13)
+    m = w.block_mask[0].numpy()
+    pairs = sum(1 for i in range(rb0, rb1) for j in range(S) if m[i // 128, j // 128] and not (causal and j > i))
+    assert flops == 4.0 * D * pairs * H

@@ -70,6 +70,9 @@ def test_parity_workload(index):
     if w.path == "bwd":
         pytest.skip("backward workloads: tests/test_gpu_bwd.py")
     q, k, v = workload_qkv(index)
+    if w.path == "blockmask":
+        _parity_blockmask_workload(w, index, q, k, v)
+        return
     win = w.window if w.window_left >= 0 else None
     og, lg = run_gpu(q, k, v, w.scale, w.causal, window=win,
                      splits=0 if w.path == "splitkv" else None)
@@ -87,6 +90,34 @@ def test_parity_workload(index):
     assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
     vmax = v.float().amax(dim=2, keepdim=True).double().numpy()
     vmin = v.float().amin(dim=2, keepdim=True).double().numpy()
+    assert np.all(og <= vmax + 2e-2) and np.all(og >= vmin - 2e-2)
+
+
+def _parity_blockmask_workload(w, index, q, k, v):
+    """The block-mask workload in the benchmark's launch (its pattern and pairing
+    stride): whole query blocks of a few heads (first, second and last blocks
+    among them) against the block-mask oracle on those rows with every key, and
+    at every element the convex-combination bound."""
+    mask = w.block_mask
+    o, l = fa.fa_fwd_blockmask(q.cuda(), k.cuda(), v.cuda(), mask.cuda(), w.window[0], w.window[1],
+                               scale=w.scale, pair_stride=w.dilation)
+    torch.cuda.synchronize()
+    BH, Bq = w.B * w.H, 128
+    og = o.float().cpu().double().numpy().reshape(BH, w.Sq, w.D)
+    lg = l.cpu().double().numpy().reshape(BH, w.Sq)
+    qb, kb, vb = (bf16_bits(t).reshape(BH, -1, w.D) for t in (q, k, v))
+    rng = np.random.default_rng(index)
+    n_qb = -(-w.Sq // Bq)
+    for bh in sorted(set([0, BH - 1] + [int(x) for x in rng.integers(0, BH, 2)])):
+        for a in sorted(set([0, 1, n_qb - 1] + [int(x) for x in rng.integers(0, n_qb, 2)])):
+            rows = slice(a * Bq, min(w.Sq, a * Bq + Bq))
+            win = (-1, a * Bq) if w.causal else (-1, -1)
+            ro, rl = oracle.attn_fwd_blockmask(qb[bh][rows][None, None], kb[bh][None, None], vb[bh][None, None],
+                                               w.scale, mask.numpy()[:, a:a + 1], window=win, block=(Bq, Bq))
+            compare(og[bh][rows], lg[bh][rows], ro[0, 0], rl[0, 0], f"{w.name} head {bh} block {a}")
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg))
+    vmax = v.float().amax(dim=2).double().numpy().reshape(BH, 1, w.D)
+    vmin = v.float().amin(dim=2).double().numpy().reshape(BH, 1, w.D)
     assert np.all(og <= vmax + 2e-2) and np.all(og >= vmin - 2e-2)
 
 
