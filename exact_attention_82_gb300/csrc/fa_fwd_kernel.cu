@@ -182,9 +182,9 @@ struct Item {
     int J, N;
     int first[2], last[2];
     // Block mask: mrow[t] is sub-tile t's row of the mask (null: every tile of
-    // its range [jlo, jhi] taken -- no mask, or a row that keeps a contiguous run).  A sub-tile whose row keeps no
-    // tile of its range takes part in one tile with every key masked ("none"),
-    // so that its rows come out as O = 0, LSE = -inf through the usual path.
+    // its range [jlo, jhi] taken -- no mask, or a row that keeps a contiguous
+    // run).  A sub-tile whose row keeps no tile of its range ("none") takes part,
+    // unmasked, in one loaded tile, and its rows are written as O = 0, LSE = -inf.
     const unsigned char *mrow[2];
     bool none[2];
     int cnt[2];  // (block mask) tiles sub-tile t takes part in
@@ -935,7 +935,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(s_tm + 96, s[3]);
                 // A tile needs the mask unless every row of the sub-tile may see all
                 // of its keys (causal: only the diagonal tile; ragged: the last).
-                // A sub-tile whose block-mask row keeps nothing masks every key.
                 if constexpr (MASK) {
                     do {
                         --jt;
