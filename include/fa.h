@@ -123,8 +123,8 @@ int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *l
  *               blocks a and a + pair_stride are computed together (in groups
  *               of 2 * pair_stride blocks; the last blocks with their
  *               neighbours) and share the loads of the key blocks either keeps.
- *               1 suits masks whose neighbouring rows keep like blocks (bands,
- *               random masks); a dilated pattern with stride r wants r.
+ *               1 suits masks whose neighbouring block rows keep like blocks
+ *               (bands, local patterns); a dilated pattern with stride r wants r.
  * Other arguments, layout, ownership and outputs are those of fa_fwd_window.
  * A query row with no allowed key (its block row keeps nothing, or the band
  * leaves nothing of what it keeps) gets O = 0 and LSE = -inf.
