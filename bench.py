@@ -306,7 +306,7 @@ def run_ours(args, rank, world, local_rank):
     w_full = WORKLOADS[args.workload]
     # this rank's part: the whole workload, or (--split heads) its block of heads
     w, h0, nh = rank_workload(w_full, world, rank, args.split)
-    if args.split == "heads" and w_full.path not in ("fwd", "fp8"):
+    if args.split == "heads" and w_full.path not in ("fwd", "fp8", "blockmask"):
         raise SystemExit("--split heads applies to the forward workloads")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)

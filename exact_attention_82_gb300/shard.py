@@ -38,20 +38,27 @@ def head_slice(t, start: int, count: int):
 
 
 def fa_fwd_shard(q, k, v, o, lse, rank: int, world: int, scale: float | None = None,
-                 causal: bool = False, window=None, stream=None):
+                 causal: bool = False, window=None, stream=None, block_mask=None, pair_stride: int = 1):
     """This rank's share of the forward over whole [B, H, S, D] tensors: the
     heads head_range(B*H, world, rank) of O and LSE are written, no other row
     is touched.  q, k, v, o, lse are CUDA tensors as fa_fwd takes them;
-    `window` = (window_left, window_right) selects the banded call.  Returns
+    `window` = (window_left, window_right) selects the banded call, and
+    `block_mask` ([1 or B*H, n_qb, n_kb], as fa_fwd_blockmask takes it; a
+    per-head mask is cut to the rank's heads) the block-mask call.  Returns
     (start, count)."""
-    from . import fa_fwd, fa_fwd_window
+    from . import fa_fwd, fa_fwd_blockmask, fa_fwd_window
 
     B, H = q.shape[0], q.shape[1]
     start, count = head_range(B * H, world, rank)
     if count == 0:
         return start, 0
     qs, ks, vs, os_, ls = (head_slice(t, start, count) for t in (q, k, v, o, lse))
-    if window is None:
+    if block_mask is not None:
+        ms = block_mask if block_mask.shape[0] == 1 else block_mask[start:start + count]
+        wl, wr = window if window is not None else (-1, 0 if causal else -1)
+        fa_fwd_blockmask(qs, ks, vs, ms, wl, wr, o=os_, lse=ls, scale=scale, pair_stride=pair_stride,
+                         stream=stream)
+    elif window is None:
         fa_fwd(qs, ks, vs, o=os_, lse=ls, scale=scale, causal=causal, stream=stream)
     else:
         fa_fwd_window(qs, ks, vs, window[0], window[1], o=os_, lse=ls, scale=scale, stream=stream)

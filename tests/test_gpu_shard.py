@@ -42,3 +42,27 @@ def test_split_heads_equal_one_call(world, causal, D, window):
         assert torch.isnan(of[done:]).all() and torch.isnan(lf[done:]).all()  # later ranks' rows untouched
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
     assert fa.fa_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("per_head,causal,stride", [(True, False, 1), (False, True, 2)])
+def test_split_heads_block_mask_equal_one_call(world, per_head, causal, stride):
+    from exact_attention_82_gb300.inputs import dilated_block_mask, random_block_mask
+
+    B, H, S, D = 1, 6, 700, 128
+    q, k, v = (t.cuda() for t in make_qkv(B, H, S, S, D, seed=56))
+    n = -(-S // 128)
+    mask = (random_block_mask(B * H, n, n, 0.5, 57) if per_head else dilated_block_mask(n, n, 2, causal)).cuda()
+    o_ref, lse_ref = fa.fa_fwd_blockmask(q, k, v, mask, -1, 0 if causal else -1, pair_stride=stride)
+    o = torch.full_like(o_ref, float("nan"))
+    lse = torch.full_like(lse_ref, float("nan"))
+    for rank in range(world):
+        start, count = fa_fwd_shard(q, k, v, o, lse, rank, world, causal=causal, block_mask=mask,
+                                    pair_stride=stride)
+        assert (start, count) == head_range(B * H, world, rank)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref)
+    assert torch.equal(torch.isneginf(lse), torch.isneginf(lse_ref))
+    fin = torch.isfinite(lse_ref)
+    assert torch.equal(lse[fin], lse_ref[fin])
+    assert fa.fa_device_status() == fa.FA_OK
