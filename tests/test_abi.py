@@ -151,6 +151,13 @@ def test_blockmask_argument_checks():
     assert "mask" in fa.fa_strerror(fa.FA_ERR_BAD_MASK)
 
 
+def test_blockmask_wrapper_rejects_bad_masks_before_the_call():
+    q = torch.zeros(1, 1, 300, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # CPU tensors
+        fa.fa_fwd_blockmask(q, q, q, torch.ones(1, 3, 3, dtype=torch.uint8), o=q.clone(),
+                            lse=torch.zeros(1, 1, 300), stream=0)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path only")
 def test_blockmask_valid_call_without_gpu_reports_cuda_error():
     assert mcall(heads=3, B=1, H=3) == fa.FA_ERR_CUDA
