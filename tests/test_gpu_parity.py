@@ -63,7 +63,7 @@ def test_parity_other_scale():
     full_parity(1, 2, 257, 257, 128, False, seed=5, scale=0.3)
 
 
-# --------------------------------------------------- the five workloads
+# ------------------------------------------------ the benchmark's workloads
 @pytest.mark.parametrize("index", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
 def test_parity_workload(index):
     w = WORKLOADS[index]
